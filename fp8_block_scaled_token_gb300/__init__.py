@@ -1,1 +1,243 @@
-"""Small-M FP8 block-scaled linear layer for GB300 (sm_103a)."""
+"""Small-M FP8 block-scaled linear layer for GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``lib/libfp8bs.so`` (declared in
+``include/fp8bs.h``).  This module only marshals arguments: torch tensors
+provide device memory and the current CUDA stream; every step of the layer
+runs in the library's CUDA kernels.  There is no fallback: if the library is
+missing or a call fails, a RuntimeError says why.
+
+Entry points (same names as the C ABI):
+
+* ``fp8_quant_act(x)`` -> (xq, xs): per-token, per-128 E4M3 cast of bf16 X.
+* ``fp8_quant_weight_blocks(w)`` -> (wq, ws): 128x128-block E4M3 weights.
+* ``fp8_blockscaled_gemm(aq, as_, wq, ws)`` -> Y bf16.
+* ``fp8_blockscaled_gemm_fused(x, wq, ws)`` -> Y bf16 (cast fused in).
+* ``bf16_gemm_ref(x, w)`` -> Y bf16 (the 16-bit output-layer baseline).
+"""
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "lib", "libfp8bs.so")
+
+FLAG_OVERLAP_PREV = 1
+F32, BF16 = 0, 1
+
+_lib = None
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn, code, text):
+        super().__init__("%s failed: %s (status %d)" % (fn, text, code))
+        self.code = code
+
+
+def lib():
+    """The loaded libfp8bs.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libfp8bs.so is not built (expected at %s); run "
+                           "`python -c \"import __graft_entry__ as g; g.build()\"`" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, u, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+    L.fp8bs_status_string.restype = ctypes.c_char_p
+    L.fp8bs_status_string.argtypes = [i]
+    sigs = {
+        "fp8_quant_act": [vp, i, i, i, vp, vp, u, vp],
+        "fp8_quant_weight_blocks": [vp, i, i, i, vp, vp, vp],
+        "fp8_blockscaled_gemm_workspace_size": [i, i, i, ctypes.POINTER(sz)],
+        "fp8_blockscaled_gemm": [vp, vp, vp, vp, vp, i, i, i, vp, sz, u, vp],
+        "fp8_blockscaled_gemm_fused": [vp, i, vp, vp, vp, i, i, i, vp, sz, u, vp],
+        "bf16_gemm_ref_workspace_size": [i, i, i, ctypes.POINTER(sz)],
+        "bf16_gemm_ref": [vp, vp, vp, i, i, i, vp, sz, u, vp],
+        "fp8bs_workspace_status": [vp, i, ctypes.POINTER(i)],
+        "fp8bs_split_plan": [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_longlong),
+                             ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)],
+        "fp8bs_testhook_gemm_stall": [vp, vp, vp, vp, vp, i, i, i, vp, sz, i, ctypes.c_ulonglong, vp],
+    }
+    for name, args in sigs.items():
+        f = getattr(L, name)
+        f.restype = i
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(code):
+    return lib().fp8bs_status_string(int(code)).decode()
+
+
+def _check(fn, code):
+    if code != 0:
+        raise Fp8bsError(fn, code, status_string(code))
+
+
+# ---------------------------------------------------------------- helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream():
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, dtype, name, ndim=2):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor (there is no CPU path)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != ndim:
+        raise ValueError("%s must be %d-D" % (name, ndim))
+
+
+def _rows_contiguous(t, name):
+    if t.stride(-1) != 1:
+        raise ValueError("%s must have unit stride along K" % name)
+
+
+# ---------------------------------------------------------------- entry points
+def fp8_quant_act(x, xq=None, xs=None, flags=0):
+    """bf16 X [M, K] (row stride may exceed K) -> (xq uint8 [M,K], xs fp32 [M,K/128])."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    _rows_contiguous(x, "x")
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if xs is None:
+        xs = torch.empty((M, max(K // 128, 0)), dtype=torch.float32, device=x.device)
+    _check("fp8_quant_act", lib().fp8_quant_act(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(xs), flags, _stream()))
+    return xq, xs
+
+
+def fp8_quant_weight_blocks(w, wq=None, ws=None):
+    """fp32 or bf16 W [N, K] -> (wq uint8 [N,K], ws fp32 [ceil(N/128), K/128])."""
+    torch = _torch()
+    if w.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("w must be float32 or bfloat16")
+    _need(w, w.dtype, "w")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    N, K = w.shape
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if ws is None:
+        ws = torch.empty(((N + 127) // 128, max(K // 128, 0)), dtype=torch.float32, device=w.device)
+    wt = BF16 if w.dtype == torch.bfloat16 else F32
+    _check("fp8_quant_weight_blocks", lib().fp8_quant_weight_blocks(_ptr(w), wt, N, K, _ptr(wq), _ptr(ws), _stream()))
+    return wq, ws
+
+
+def fp8_blockscaled_gemm_workspace_size(M, N, K):
+    n = ctypes.c_size_t(0)
+    _check("fp8_blockscaled_gemm_workspace_size", lib().fp8_blockscaled_gemm_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def bf16_gemm_ref_workspace_size(M, N, K):
+    n = ctypes.c_size_t(0)
+    _check("bf16_gemm_ref_workspace_size", lib().bf16_gemm_ref_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def make_workspace(nbytes, device=None):
+    """A zero-filled, 256-byte aligned device workspace of ``nbytes``."""
+    torch = _torch()
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def fp8_blockscaled_gemm(aq, as_, wq, ws, y=None, workspace=None, flags=0):
+    """Y[M,N] bf16 from pre-quantised operands."""
+    torch = _torch()
+    _need(aq, torch.uint8, "aq")
+    _need(as_, torch.float32, "as_")
+    _need(wq, torch.uint8, "wq")
+    _need(ws, torch.float32, "ws")
+    for t, n in ((aq, "aq"), (as_, "as_"), (wq, "wq"), (ws, "ws")):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    M, K = aq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K or tuple(as_.shape) != (M, K // 128) or tuple(ws.shape) != ((N + 127) // 128, K // 128):
+        raise ValueError("operand shapes do not agree")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    if workspace is None:
+        workspace = make_workspace(fp8_blockscaled_gemm_workspace_size(M, N, K), aq.device)
+    _check("fp8_blockscaled_gemm",
+           lib().fp8_blockscaled_gemm(_ptr(aq), _ptr(as_), _ptr(wq), _ptr(ws), _ptr(y), M, N, K,
+                                      _ptr(workspace), workspace.numel(), flags, _stream()))
+    return y
+
+
+def fp8_blockscaled_gemm_fused(x, wq, ws, y=None, workspace=None, flags=0):
+    """Y[M,N] bf16 from bf16 activations (row stride may exceed K)."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    _rows_contiguous(x, "x")
+    _need(wq, torch.uint8, "wq")
+    _need(ws, torch.float32, "ws")
+    M, K = x.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K or tuple(ws.shape) != ((N + 127) // 128, K // 128):
+        raise ValueError("operand shapes do not agree")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = make_workspace(fp8_blockscaled_gemm_workspace_size(M, N, K), x.device)
+    _check("fp8_blockscaled_gemm_fused",
+           lib().fp8_blockscaled_gemm_fused(_ptr(x), x.stride(0), _ptr(wq), _ptr(ws), _ptr(y), M, N, K,
+                                            _ptr(workspace), workspace.numel(), flags, _stream()))
+    return y
+
+
+def bf16_gemm_ref(x, w, y=None, workspace=None, flags=0):
+    """Y[M,N] bf16 = X bf16 [M,K] . W bf16 [N,K]^T (fp32 accumulation)."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    if not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("operand shapes do not agree")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = make_workspace(bf16_gemm_ref_workspace_size(M, N, K), x.device)
+    _check("bf16_gemm_ref",
+           lib().bf16_gemm_ref(_ptr(x), _ptr(w), _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
+                               flags, _stream()))
+    return y
+
+
+def workspace_status(workspace, clear=False):
+    """Device-side failure word of a workspace (synchronises the device)."""
+    code = ctypes.c_int(0)
+    rc = lib().fp8bs_workspace_status(_ptr(workspace), 1 if clear else 0, ctypes.byref(code))
+    if rc not in (0, 7):
+        _check("fp8bs_workspace_status", rc)
+    return code.value
+
+
+def split_plan(N, K, bf16=False, num_sms=0, cta=-1):
+    """(ctas, units, unit_begin, unit_end) of the K-split schedule."""
+    c = ctypes.c_int(0)
+    u = ctypes.c_longlong(0)
+    b = ctypes.c_longlong(0)
+    e = ctypes.c_longlong(0)
+    _check("fp8bs_split_plan", lib().fp8bs_split_plan(N, K, 1 if bf16 else 0, num_sms, cta, ctypes.byref(c),
+                                                      ctypes.byref(u), ctypes.byref(b), ctypes.byref(e)))
+    return c.value, u.value, (b.value if cta >= 0 else None), (e.value if cta >= 0 else None)

@@ -1,0 +1,461 @@
+// gemm_kernel.cuh -- swap-AB, K-split GEMM for small M on sm_103a.
+//
+// Y[M,N] = dequant(Aq[M,K]) . dequant(Wq[N,K])^T with W in 128x128 fp32
+// block scales and A in 1x128 fp32 group scales ("A 23% faster GPU kernel, and
+// a model that did not move", "Why this shape is hard"), plus the same
+// pipeline for the 16-bit output-layer baseline ("The profiler said the kernel
+// ran zero times", "The output layer, which did run").
+//
+// Design (one CTA per SM, warp-specialised):
+//   warp 0      TMA producer: streams 128x128-byte weight tiles (and, when
+//               the activations are pre-quantised, the token tile) into an
+//               S-stage shared-memory ring, 128-byte swizzled, no multicast.
+//   warp 1      MMA issuer: per 128-wide K block, four tcgen05.mma with the
+//               weights as the 128-row A operand and the tokens (padded to
+//               NPAD = 16/32/48/64) as the B operand, fp32 accumulator in
+//               tensor memory (4 buffers so the epilogue never stalls it).
+//   warps 2-5   promotion / epilogue: one thread per weight row reads its
+//               accumulator row (tcgen05.ld), multiplies by
+//               s_w[tile,kb] * s_a[m,kb] and adds into fp32 registers; at the
+//               end of a tile it stores bf16 Y, or hands its partial to the
+//               fixed-order K-split reduction.
+//   warps 6-9   (fused variant only) activation quantisation: each warp takes
+//               every 4th unit, reads the bf16 token rows of that K block,
+//               computes the per-token scale and writes E4M3 codes straight
+//               into the swizzled B-operand tile of the ring stage.
+//
+// Every wait is bounded; on time-out the CTA records a code in the status
+// word, drains what it has in flight, frees its tensor memory and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "plan.cuh"
+#include "ptx.cuh"
+#include "quant_math.cuh"
+
+namespace fp8bs {
+
+enum GemmMode : int {
+    kModeFp8 = 0,      // pre-quantised activations (Aq, s_a) read by TMA
+    kModeFp8Fused = 1, // bf16 activations quantised inside the kernel
+    kModeBf16 = 2,     // bf16 x bf16, no block scales
+};
+
+struct GemmParams {
+    int M, N, K;
+    int kg;          // K blocks per tile (K/128 for FP8, K/64 for bf16)
+    int ntiles;      // ceil(N / 128)
+    long long units; // ntiles * kg
+    int ctas;
+    const float *as;         // FP8: s_a [M][K/128]
+    const float *ws;         // FP8: s_w [ntiles][K/128]
+    const uint16_t *x;       // fused: bf16 activations [M][ldx]
+    int ldx;
+    uint16_t *y;             // bf16 [M][N]
+    unsigned *status;        // workspace word 0
+    unsigned *counters;      // [ntiles] arrival counters, zero between calls
+    float *slots;            // [2 * ctas][NPAD * 128] fp32 partials
+    int prefetch_before_wait;// weights may be fetched before the previous grid completes
+    int test_skip_unit;      // -1, or a unit whose stage the producer never fills
+    unsigned long long timeout_ns;
+};
+
+template <int NPAD, int MODE> struct GemmCfg {
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "token tile");
+    static constexpr int kTileRows = 128;                   // weight rows per tile (MMA M)
+    static constexpr int kRowBytes = 128;                   // K bytes per row per stage
+    static constexpr int kChunkElems = MODE == kModeBf16 ? 64 : 128;
+    static constexpr int kWBytes = kTileRows * kRowBytes;   // 16 KB
+    static constexpr int kBBytes = NPAD * kRowBytes;        // 2..8 KB
+    static constexpr int kStageBytes = kWBytes + kBBytes;   // multiple of 1024
+    static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
+    static constexpr int kAcc = 4;
+    static constexpr int kTmemNeed = kAcc * NPAD;
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
+    static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
+    static constexpr int kEpiWarps = 4;
+    static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
+    static constexpr int kSaOffset = kStages * kStageBytes;
+    static constexpr int kSaBytes = MODE == kModeFp8Fused ? kStages * 64 * 4 : 0;
+    static constexpr int kBarOffset = kSaOffset + kSaBytes;
+    static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
+    static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024; // +1024: runtime alignment
+    static constexpr int kMmaSteps = kRowBytes / 32;        // 32 bytes of K per tcgen05.mma
+    static constexpr uint32_t kIdesc =
+        MODE == kModeBf16 ? idesc_bf16_f32(kTileRows, NPAD) : idesc_e4m3_f32(kTileRows, NPAD);
+    static_assert(kStageBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    static_assert(kStages >= 5, "the fused quant warps rely on a ring of at least 5 stages");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+template <int NPAD, int MODE>
+__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
+    gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
+                        const GemmParams p)
+{
+    using C = GemmCfg<NPAD, MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;
+    uint64_t *tempty = tfull + C::kAcc;
+    uint64_t *mma_done = tempty + C::kAcc;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
+    float *sa_ring = reinterpret_cast<float *>(smem + C::kSaOffset);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const long long u0 = plan_begin(p.units, p.ctas, cta);
+    const int nunits = static_cast<int>(plan_begin(p.units, p.ctas, cta + 1) - u0);
+    const int kg = p.kg;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], MODE == kModeFp8Fused ? 2 : 1);
+            mbar_init(&empty[s], MODE == kModeFp8Fused ? 1 + C::kEpiWarps : 1);
+        }
+        for (int a = 0; a < C::kAcc; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], C::kEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_w);
+        if (MODE != kModeFp8Fused)
+            prefetch_tmap(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (MODE == kModeFp8Fused) {
+        // Token rows >= M of every B tile, and their scales, stay zero for the
+        // whole kernel.
+        for (int i = threadIdx.x; i < C::kStages * (C::kBBytes / 16); i += C::kThreads) {
+            const int s = i / (C::kBBytes / 16), o = i % (C::kBBytes / 16);
+            reinterpret_cast<uint4 *>(smem + s * C::kStageBytes + C::kWBytes)[o] = make_uint4(0, 0, 0, 0);
+        }
+        for (int i = threadIdx.x; i < C::kStages * 64; i += C::kThreads)
+            sa_ring[i] = 0.0f;
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (threadIdx.x == 0)
+        grid_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_b = l2_policy_evict_last();
+            const uint32_t tx = C::kWBytes + (MODE == kModeFp8Fused ? 0 : C::kBBytes);
+            uint32_t armed_mask = 0, armed_parity = 0;
+            const int pre = p.prefetch_before_wait ? (nunits < C::kStages ? nunits : C::kStages) : 0;
+            // Weights for the first ring pass, possibly before the previous grid is done.
+            for (int i = 0; i < pre; ++i) {
+                if (i == p.test_skip_unit)
+                    continue;
+                const long long u = u0 + i;
+                const int tile = static_cast<int>(u / kg), kb = static_cast<int>(u % kg);
+                mbar_arrive_expect_tx(&full[i], tx);
+                armed_mask |= 1u << i;
+                tma_load_2d(smem + i * C::kStageBytes, &tm_w, &full[i], kb * C::kChunkElems,
+                            tile * C::kTileRows, pol_w);
+            }
+            grid_dependency_wait();
+            if (MODE != kModeFp8Fused) {
+                for (int i = 0; i < pre; ++i) {
+                    if (i == p.test_skip_unit)
+                        continue;
+                    const int kb = static_cast<int>((u0 + i) % kg);
+                    tma_load_2d(smem + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb * C::kChunkElems, 0,
+                                pol_b);
+                }
+            }
+            for (int i = pre; i < nunits; ++i) {
+                const int s = i % C::kStages;
+                const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutProducer, p.timeout_ns))
+                    break;
+                if (i == p.test_skip_unit)
+                    continue;
+                const long long u = u0 + i;
+                const int tile = static_cast<int>(u / kg), kb = static_cast<int>(u % kg);
+                mbar_arrive_expect_tx(&full[s], tx);
+                armed_mask |= 1u << s;
+                armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                tma_load_2d(smem + s * C::kStageBytes, &tm_w, &full[s], kb * C::kChunkElems, tile * C::kTileRows,
+                            pol_w);
+                if (MODE != kModeFp8Fused)
+                    tma_load_2d(smem + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems, 0,
+                                pol_b);
+            }
+            // Nothing may still be landing in shared memory when the CTA exits:
+            // wait (bounded) for the last phase armed on every stage.
+            for (int s = 0; s < C::kStages; ++s) {
+                if (!(armed_mask & (1u << s)))
+                    continue;
+                const uint32_t ph = (armed_parity >> s) & 1u;
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_test(&full[s], ph)) {
+                    if (globaltimer_ns() - t0 > p.timeout_ns) {
+                        atomicOr(p.status, kErrTimeoutDrain);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int acc = 0;
+            uint32_t acc_ph = 0;
+            for (int i = 0; i < nunits; ++i) {
+                const int s = i % C::kStages;
+                const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
+                const int kb = static_cast<int>((u0 + i) % kg);
+                const bool seg_start = (i == 0) || (kb == 0);
+                const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
+                // FP8: every K block gets a fresh accumulator (its scale differs);
+                // bf16: one accumulator per tile segment.
+                const bool fresh = (MODE != kModeBf16) || seg_start;
+                const bool publish = (MODE != kModeBf16) || seg_end;
+                if (fresh && !mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, p.status, kErrTimeoutMma,
+                                        p.timeout_ns))
+                    break;
+                if (!mbar_wait(&full[s], ph, abort_flag, p.status, kErrTimeoutMma, p.timeout_ns))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NPAD);
+                const uint64_t a_desc = sw128_kmajor_desc(smem_u32(smem + s * C::kStageBytes));
+                const uint64_t b_desc = sw128_kmajor_desc(smem_u32(smem + s * C::kStageBytes + C::kWBytes));
+#pragma unroll
+                for (int k = 0; k < C::kMmaSteps; ++k) {
+                    const uint32_t accumulate = (k > 0 || !fresh) ? 1u : 0u;
+                    if (MODE == kModeBf16)
+                        mma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, C::kIdesc, accumulate);
+                    else
+                        mma_f8f6f4(d_tmem, a_desc + 2 * k, b_desc + 2 * k, C::kIdesc, accumulate);
+                }
+                mma_commit(&empty[s]);
+                if (publish) {
+                    mma_commit(&tfull[acc]);
+                    if (++acc == C::kAcc) {
+                        acc = 0;
+                        acc_ph ^= 1u;
+                    }
+                }
+            }
+            // Every MMA this thread issued must be complete before the
+            // tensor memory is released.
+            mma_commit(mma_done);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_test(mma_done, 0)) {
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    atomicOr(p.status, kErrTimeoutDrain);
+                    break;
+                }
+            }
+        }
+    } else if (warp < 2 + C::kEpiWarps) {
+        // ------------------------------------------------ promotion / epilogue
+        const int quarter = warp & 3;             // TMEM lanes this warp may read
+        const int row = quarter * 32 + lane;      // weight row within the tile
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        float acc[NPAD];
+#pragma unroll
+        for (int m = 0; m < NPAD; ++m)
+            acc[m] = 0.0f;
+        int accb = 0;
+        uint32_t acc_ph = 0;
+        int seg_first_kb = 0;
+        grid_dependency_wait();
+        for (int i = 0; i < nunits; ++i) {
+            const long long u = u0 + i;
+            const int tile = static_cast<int>(u / kg), kb = static_cast<int>(u % kg);
+            const bool seg_start = (i == 0) || (kb == 0);
+            const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
+            const int s = i % C::kStages;
+            if (seg_start)
+                seg_first_kb = kb;
+            if (MODE != kModeBf16 || seg_end) {
+                float sw = 1.0f, sa0 = 0.0f, sa1 = 0.0f;
+                if (MODE != kModeBf16)
+                    sw = p.ws[static_cast<long long>(tile) * kg + kb];
+                if (MODE == kModeFp8) {
+                    if (lane < p.M)
+                        sa0 = p.as[static_cast<long long>(lane) * kg + kb];
+                    if (lane + 32 < p.M)
+                        sa1 = p.as[static_cast<long long>(lane + 32) * kg + kb];
+                }
+                mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
+                if (MODE == kModeFp8Fused) {
+                    // Acquire the quantisation warp's writes of this stage's
+                    // scales (that phase is complete once the MMA has run).
+                    mbar_wait(&full[s], static_cast<uint32_t>(i / C::kStages) & 1u, abort_flag, p.status,
+                              kErrTimeoutEpilogue, p.timeout_ns);
+                }
+                named_bar_sync(1, 32 * C::kEpiWarps);
+                if (*abort_flag)
+                    break; // uniform across the four epilogue warps
+                tc_fence_after_sync();
+                const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD);
+#pragma unroll
+                for (int c = 0; c < NPAD / 16; ++c) {
+                    uint32_t r[16];
+                    tmem_load16(taddr + c * 16, r);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = c * 16 + j;
+                        const float d = __uint_as_float(r[j]);
+                        if (MODE == kModeBf16) {
+                            acc[m] = d;
+                        } else {
+                            float sam;
+                            if (MODE == kModeFp8Fused)
+                                sam = sa_ring[s * 64 + m];
+                            else
+                                sam = __shfl_sync(0xffffffffu, m < 32 ? sa0 : sa1, m & 31);
+                            acc[m] = fmaf(sw * sam, d, acc[m]);
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&tempty[accb]);
+                    if (MODE == kModeFp8Fused)
+                        mbar_arrive(&empty[s]);
+                }
+                if (++accb == C::kAcc) {
+                    accb = 0;
+                    acc_ph ^= 1u;
+                }
+            }
+            if (!seg_end)
+                continue;
+            // ---- tile segment complete: store or reduce
+            const int n = tile * C::kTileRows + row;
+            const bool whole_tile = (seg_first_kb == 0) && (kb == kg - 1);
+            if (whole_tile) {
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < NPAD; ++m)
+                        if (m < p.M)
+                            p.y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                }
+            } else {
+                const long long t_first = static_cast<long long>(tile) * kg;
+                const int c_first = plan_owner(p.units, p.ctas, t_first);
+                const int c_last = plan_owner(p.units, p.ctas, t_first + kg - 1);
+                float *mine = p.slots + static_cast<long long>(plan_slot(p.units, p.ctas, kg, cta, tile)) * (NPAD * 128);
+#pragma unroll
+                for (int m = 0; m < NPAD; ++m)
+                    if (m < p.M)
+                        mine[m * 128 + row] = acc[m];
+                __threadfence();
+                named_bar_sync(1, 32 * C::kEpiWarps);
+                if (warp == 2 && lane == 0) {
+                    const unsigned prev = atomicAdd(&p.counters[tile], 1u);
+                    *last_flag = (prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
+                }
+                named_bar_sync(1, 32 * C::kEpiWarps);
+                if (*last_flag) {
+                    // Sum every contributor's slot (this CTA's included) in
+                    // contributor order, whatever the arrival order was.
+                    __threadfence();
+#pragma unroll
+                    for (int m = 0; m < NPAD; ++m)
+                        acc[m] = 0.0f;
+                    for (int c = c_first; c <= c_last; ++c) {
+                        const float *src =
+                            p.slots + static_cast<long long>(plan_slot(p.units, p.ctas, kg, c, tile)) * (NPAD * 128);
+#pragma unroll
+                        for (int m = 0; m < NPAD; ++m)
+                            if (m < p.M)
+                                acc[m] += __ldcg(src + m * 128 + row);
+                    }
+                    if (n < p.N) {
+#pragma unroll
+                        for (int m = 0; m < NPAD; ++m)
+                            if (m < p.M)
+                                p.y[static_cast<long long>(m) * p.N + n] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                    }
+                    if (warp == 2 && lane == 0)
+                        p.counters[tile] = 0u; // ready for the next call
+                }
+                named_bar_sync(1, 32 * C::kEpiWarps);
+            }
+#pragma unroll
+            for (int m = 0; m < NPAD; ++m)
+                acc[m] = 0.0f;
+        }
+    } else {
+        // ------------------------------------------------ fused activation quantisation
+        if constexpr (MODE == kModeFp8Fused) {
+            const int qw = warp - 2 - C::kEpiWarps;
+            grid_dependency_wait();
+            for (int i = qw; i < nunits; i += C::kQuantWarps) {
+                const int s = i % C::kStages;
+                const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutQuant, p.timeout_ns))
+                    break;
+                const int kb = static_cast<int>((u0 + i) % kg);
+                const uint16_t *xk = p.x + static_cast<long long>(kb) * 128 + lane * 4;
+                uint8_t *btile = smem + s * C::kStageBytes + C::kWBytes;
+                for (int m0 = 0; m0 < p.M; m0 += 8) {
+                    uint2 raw[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (m0 + j < p.M)
+                            raw[j] = *reinterpret_cast<const uint2 *>(xk + static_cast<long long>(m0 + j) * p.ldx);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int m = m0 + j;
+                        if (m < p.M) {
+                            uint32_t codes;
+                            const float sc = quant_group_warp(raw[j], codes);
+                            // row m, bytes 4*lane..4*lane+3 of the 128-byte row; the 16-byte
+                            // chunk index is XOR-ed with (row mod 8) as TMA's 128-byte swizzle does.
+                            const uint32_t off =
+                                static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) + ((lane & 3) << 2));
+                            *reinterpret_cast<uint32_t *>(btile + off) = codes;
+                            if (lane == 0)
+                                sa_ring[s * 64 + m] = sc;
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&full[s]);
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+} // namespace fp8bs

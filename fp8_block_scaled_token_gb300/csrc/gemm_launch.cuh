@@ -1,0 +1,94 @@
+// gemm_launch.cuh -- host launch of gemm_small_m_kernel for one mode; each
+// gemm_*.cu translation unit instantiates it for its mode so the four token
+// widths of the three modes compile in parallel.
+#pragma once
+
+#include "gemm_kernel.cuh"
+#include "internal.h"
+
+namespace fp8bs {
+
+template <int NPAD, int MODE>
+fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
+{
+    using C = GemmCfg<NPAD, MODE>;
+    static unsigned long long attr_done = 0;
+    auto kernel = gemm_small_m_kernel<NPAD, MODE>;
+    fp8bs_status st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), C::kSmemBytes, dev.device,
+                                       &attr_done);
+    if (st != FP8BS_OK)
+        return st;
+
+    CUtensorMap tm_w, tm_b;
+    if (MODE == kModeBf16) {
+        st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.N),
+                          static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K) * 2, 64, 128);
+        if (st == FP8BS_OK)
+            st = make_tmap_2d(&tm_b, L.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.M),
+                              static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.lda) * 2, 64, NPAD);
+    } else {
+        st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.N),
+                          static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K), 128, 128);
+        if (st == FP8BS_OK) {
+            if (MODE == kModeFp8)
+                st = make_tmap_2d(&tm_b, L.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.M),
+                                  static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.lda), 128, NPAD);
+            else
+                tm_b = tm_w; // unused by the fused kernel
+        }
+    }
+    if (st != FP8BS_OK)
+        return st;
+
+    const WorkspaceLayout wl = workspace_layout(sh.ntiles, sh.ctas, NPAD);
+    uint8_t *wsb = static_cast<uint8_t *>(L.workspace);
+    GemmParams p;
+    p.M = L.M;
+    p.N = L.N;
+    p.K = L.K;
+    p.kg = sh.kg;
+    p.ntiles = sh.ntiles;
+    p.units = sh.units;
+    p.ctas = sh.ctas;
+    p.as = L.as;
+    p.ws = L.ws;
+    p.x = static_cast<const uint16_t *>(MODE == kModeFp8Fused ? L.a : nullptr);
+    p.ldx = L.lda;
+    p.y = static_cast<uint16_t *>(L.y);
+    p.status = reinterpret_cast<unsigned *>(wsb);
+    p.counters = reinterpret_cast<unsigned *>(wsb + wl.counters_off);
+    p.slots = reinterpret_cast<float *>(wsb + wl.slots_off);
+    p.prefetch_before_wait = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
+    p.test_skip_unit = L.test_skip_unit;
+    p.timeout_ns = L.timeout_ns;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
+    return launch_status(cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_b, p));
+}
+
+template <int MODE>
+fp8bs_status launch_gemm_mode(const GemmLaunch &L, const DeviceInfo &dev)
+{
+    const GemmShape sh = gemm_shape(MODE, L.M, L.N, L.K, dev.sms);
+    switch (sh.npad) {
+    case 16:
+        return launch_gemm_npad<16, MODE>(L, dev, sh);
+    case 32:
+        return launch_gemm_npad<32, MODE>(L, dev, sh);
+    case 48:
+        return launch_gemm_npad<48, MODE>(L, dev, sh);
+    default:
+        return launch_gemm_npad<64, MODE>(L, dev, sh);
+    }
+}
+
+} // namespace fp8bs

@@ -1,0 +1,83 @@
+// internal.h -- host-side plumbing shared by the translation units of
+// libfp8bs.so (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include "../../include/fp8bs.h"
+
+namespace fp8bs {
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+// Current device's cached attributes; status FP8BS_ERR_CUDA when there is no
+// usable device, FP8BS_ERR_UNSUPPORTED_DEVICE when it is not sm_103.
+fp8bs_status current_device(DeviceInfo *out);
+
+// One-time per (kernel, device) opt-in to more than 48 KB of dynamic shared
+// memory.  `done_mask` is the caller's static per-kernel bit mask of devices.
+fp8bs_status ensure_smem_attr(const void *kernel, int bytes, int device, unsigned long long *done_mask);
+
+// 2-D tensor map for a row-major [rows][cols] matrix, box = box_cols x
+// box_rows elements, 128-byte swizzle, zero fill outside the matrix.
+fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                          uint64_t rows, uint64_t cols, uint64_t row_stride_bytes, uint32_t box_cols,
+                          uint32_t box_rows);
+
+fp8bs_status launch_status(cudaError_t e);
+
+// Token-tile width for M rows (16, 32, 48 or 64).
+inline int token_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
+
+// Workspace layout shared by the GEMM launchers:
+//   [0, 256)                status word (+ padding)
+//   [256, 256 + C)          ntiles 32-bit arrival counters, C rounded up to 256
+//   [256 + C, ...)          2 * ctas slots of NPAD * 128 fp32 partials
+struct WorkspaceLayout {
+    size_t counters_off, slots_off, total;
+};
+WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad);
+
+struct GemmLaunch {
+    int mode;                 // GemmMode
+    int M, N, K;
+    const void *a;            // mode 0: Aq u8 [M][K]; mode 1: X bf16 [M][ldx]; mode 2: X bf16 [M][K]
+    int lda;                  // row stride of `a` in elements
+    const float *as;          // mode 0
+    const void *w;            // mode 0/1: Wq u8 [N][K]; mode 2: W bf16 [N][K]
+    const float *ws;          // mode 0/1
+    void *y;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned flags;
+    cudaStream_t stream;
+    int test_skip_unit;       // -1 normally
+    unsigned long long timeout_ns;
+};
+
+// Shape and SM count -> schedule; shared by launch and size queries.
+struct GemmShape {
+    int kg, ntiles, ctas, npad;
+    long long units;
+};
+GemmShape gemm_shape(int mode, int M, int N, int K, int sms);
+
+fp8bs_status launch_gemm_fp8(const GemmLaunch &L, const DeviceInfo &dev);
+fp8bs_status launch_gemm_fused(const GemmLaunch &L, const DeviceInfo &dev);
+fp8bs_status launch_gemm_bf16(const GemmLaunch &L, const DeviceInfo &dev);
+
+fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, float *xs, bool pdl,
+                              cudaStream_t stream);
+fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws,
+                                 cudaStream_t stream);
+
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull; // one second
+
+} // namespace fp8bs

@@ -1,0 +1,130 @@
+// quant.cu -- E4M3 quantisation kernels.
+//
+// quant_act_kernel: the run-time cast of the activations to FP8, one fp32
+// scale per token per 128 consecutive K ("The profiler said the kernel ran
+// zero times", "What the trace showed": casting inputs to FP8).  One warp per
+// 128-element group; each lane converts four values.
+//
+// quant_weight_kernel: one fp32 scale per 128x128 weight block ("A 23% faster
+// GPU kernel, and a model that did not move", "Why this shape is hard"; "The
+// profiler said the kernel ran zero times", "The output layer, which did
+// run").  One CTA per block; each warp reads 16 full rows (512 contiguous
+// bytes of fp32 per row per instruction), so loads and stores are coalesced
+// and the block stays in registers between the max and the conversion.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant_math.cuh"
+
+namespace fp8bs {
+
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
+                                                        uint8_t *__restrict__ xq, float *__restrict__ xs)
+{
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int kg = K / 128;
+    const long long group = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (group >= static_cast<long long>(M) * kg)
+        return; // whole warp
+    const int lane = threadIdx.x & 31;
+    const int m = static_cast<int>(group / kg);
+    const int g = static_cast<int>(group % kg);
+    const uint2 raw = *reinterpret_cast<const uint2 *>(x + static_cast<long long>(m) * ldx + g * 128 + lane * 4);
+    uint32_t codes;
+    const float s = quant_group_warp(raw, codes);
+    *reinterpret_cast<uint32_t *>(xq + static_cast<long long>(m) * K + g * 128 + lane * 4) = codes;
+    if (lane == 0)
+        xs[static_cast<long long>(m) * kg + g] = s;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(256) quant_weight_kernel(const void *__restrict__ w, int N, int K,
+                                                           uint8_t *__restrict__ wq, float *__restrict__ ws)
+{
+    __shared__ float warp_amax[8];
+    const int kg = K / 128;
+    const long long blk = blockIdx.x;
+    const int nb = static_cast<int>(blk / kg), kb = static_cast<int>(blk % kg);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = nb * 128 + warp * 16;
+    float v[16][4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int r = r0 + j;
+        if (r < N) {
+            const long long off = static_cast<long long>(r) * K + kb * 128 + lane * 4;
+            if (kBf16) {
+                const uint2 raw = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(w) + off);
+                v[j][0] = bf16_lo(raw.x);
+                v[j][1] = bf16_hi(raw.x);
+                v[j][2] = bf16_lo(raw.y);
+                v[j][3] = bf16_hi(raw.y);
+            } else {
+                const float4 f = *reinterpret_cast<const float4 *>(static_cast<const float *>(w) + off);
+                v[j][0] = f.x;
+                v[j][1] = f.y;
+                v[j][2] = f.z;
+                v[j][3] = f.w;
+            }
+        } else {
+            v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+        }
+        amax = fmaxf(amax, abs_max4(v[j][0], v[j][1], v[j][2], v[j][3]));
+    }
+    amax = warp_max(amax);
+    if (lane == 0)
+        warp_amax[warp] = amax;
+    __syncthreads();
+    amax = warp_amax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i)
+        amax = fmaxf(amax, warp_amax[i]);
+    const float s = group_scale(amax);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int r = r0 + j;
+        if (r < N) {
+            const long long off = static_cast<long long>(r) * K + kb * 128 + lane * 4;
+            *reinterpret_cast<uint32_t *>(wq + off) = quantize4(v[j][0], v[j][1], v[j][2], v[j][3], s);
+        }
+    }
+    if (threadIdx.x == 0)
+        ws[blk] = s;
+}
+
+fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, float *xs, bool pdl,
+                              cudaStream_t stream)
+{
+    const long long groups = static_cast<long long>(M) * (K / 128);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((groups + 7) / 8), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return launch_status(cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const uint16_t *>(x), M, K, ldx,
+                                            xq, xs));
+}
+
+fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws,
+                                 cudaStream_t stream)
+{
+    const long long blocks = static_cast<long long>((N + 127) / 128) * (K / 128);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    if (wtype == FP8BS_BF16)
+        return launch_status(cudaLaunchKernelEx(&cfg, quant_weight_kernel<true>, w, N, K, wq, ws));
+    return launch_status(cudaLaunchKernelEx(&cfg, quant_weight_kernel<false>, w, N, K, wq, ws));
+}
+
+} // namespace fp8bs

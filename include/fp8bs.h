@@ -1,0 +1,213 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs.so: the small-M FP8 block-scaled linear layer
+ *
+ *     Y[M,N] = dequant(Aq[M,K]) . dequant(Wq[N,K])^T
+ *
+ * on one GB300 (sm_103a).  M is 1..64 rows (decode / speculative-verify
+ * batches), W is E4M3 with one fp32 scale per 128x128 block, the activations
+ * are cast on the fly to E4M3 with one fp32 scale per token per 128 K.
+ *
+ * Sources (page title, section):
+ *   [P1] "A 23% faster GPU kernel, and a model that did not move",
+ *        "Why this shape is hard": about 8 rows, the long dimension split
+ *        across all SMs, 128x128 block scales, deterministic reduction.
+ *   [P2] "The profiler said the kernel ran zero times",
+ *        "What the trace showed" (casting inputs to FP8 at run time) and
+ *        "The output layer, which did run" (248,320 x 5,120 output layer,
+ *        one scale per 128x128 block; the same layer in 16-bit as baseline).
+ *   [P3] "Kernel-Level Optimisations for LLM Inference and Training",
+ *        "Quantisation kernels" (E4M3 for weights and activations).
+ *
+ * Numeric contract (the pages are silent; plainest reading):
+ *   E4M3 is the "fn" encoding (bias 7, max finite 448, NaN 0x7F/0xFF).
+ *   scale = fl32(amax / 448) by IEEE fp32 division (1.0 when amax == 0);
+ *   code  = round-to-nearest-even, saturating, of fl32(x / scale); the sign of
+ *   a value that rounds to zero is kept (0x80).
+ *   Y is accumulated in fp32: each 128-wide K block's exact-product partial
+ *   is multiplied by s_a[m,kb] * s_w[n/128,kb] and summed in K order within a
+ *   CTA; K-split partials are summed in a fixed order, then rounded once to
+ *   bf16 (nearest even).  Results are bitwise reproducible on one device.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates no device memory and keeps no pointer after return.
+ *   - Row-major layouts: X bf16 [M][ldx]; Aq u8 [M][K]; s_a fp32 [M][K/128];
+ *     W fp32|bf16 [N][K]; Wq u8 [N][K]; s_w fp32 [ceil(N/128)][K/128];
+ *     Y bf16 [M][N].
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously; no call synchronises the host except
+ *     fp8bs_workspace_status().
+ *   - Arguments are checked on the host before anything is enqueued; on any
+ *     error nothing is launched and the status says why.  No C++ exception
+ *     crosses the ABI.  Thread-safe.
+ *   - Only compute capability 10.3 is accepted (FP8BS_ERR_UNSUPPORTED_DEVICE
+ *     otherwise).  There is no fallback path.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8BS_API __attribute__((visibility("default")))
+#else
+#define FP8BS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8bs_status {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = 1,         /* null pointer, size < 1, ldx < K, bad enum */
+    FP8BS_ERR_UNSUPPORTED_SHAPE = 2,   /* M > 64 (GEMMs), K % 128 != 0, sizes beyond 2^31 */
+    FP8BS_ERR_MISALIGNED = 3,          /* a pointer or row stride breaks the alignment stated below */
+    FP8BS_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the *_workspace_size() answer */
+    FP8BS_ERR_UNSUPPORTED_DEVICE = 5,  /* current device is not sm_103 */
+    FP8BS_ERR_CUDA = 6,                /* a CUDA runtime/driver call failed (launch, attribute, ...) */
+    FP8BS_ERR_DEVICE_TIMEOUT = 7       /* a kernel gave up waiting (see fp8bs_workspace_status) */
+} fp8bs_status;
+
+typedef enum fp8bs_dtype {
+    FP8BS_F32 = 0,
+    FP8BS_BF16 = 1
+} fp8bs_dtype;
+
+/* Flag for the GEMM entry points.  With it the kernel is launched with
+ * programmatic dependent launch: it may start while the previous kernel on
+ * `stream` is still finishing and begin streaming Wq/s_w (or W for the bf16
+ * GEMM) before that kernel completes; it reads everything else only after
+ * the previous kernel has completed.  The caller promises that no work still
+ * in flight on `stream` writes the weights or their scales. */
+#define FP8BS_FLAG_OVERLAP_PREV 1u
+
+/* Human-readable text of a status code (static storage, never NULL). */
+FP8BS_API const char *fp8bs_status_string(fp8bs_status status);
+
+/*
+ * Activation quantisation [P2 "What the trace showed"; P3 "Quantisation
+ * kernels"].  For every token m and every group g of 128 consecutive K:
+ *   amax = max |x[m, 128g .. 128g+127]|
+ *   xs[m*(K/128) + g] = amax == 0 ? 1.0f : fl32(amax / 448)
+ *   xq[m*K + k]       = e4m3_rn_satfinite(fl32(x[m,k] / xs[m, k/128]))
+ * x : bf16, M rows, row stride ldx elements; 16-byte aligned, ldx % 8 == 0.
+ * xq: u8 [M][K], 4-byte aligned.  xs: fp32 [M][K/128], 4-byte aligned.
+ * M >= 1, K >= 128, K % 128 == 0, ldx >= K.
+ * Any `flags` value other than 0 and FP8BS_FLAG_OVERLAP_PREV is rejected;
+ * with the flag the kernel is launched with programmatic dependent launch and
+ * waits for the previous kernel before it reads x.
+ */
+FP8BS_API fp8bs_status fp8_quant_act(const void *x, int M, int K, int ldx,
+                           uint8_t *xq, float *xs,
+                           unsigned flags, void *stream);
+
+/*
+ * Weight quantisation, one fp32 scale per 128x128 block [P1 "Why this shape
+ * is hard"; P2 "The output layer, which did run"].  Run once per weight.
+ * For block (nb, kb) over the rows nb*128 .. min(N, nb*128+128)-1 that exist:
+ *   amax = max |w| over the block
+ *   ws[nb*(K/128) + kb] = amax == 0 ? 1.0f : fl32(amax / 448)
+ *   wq[n*K + k] = e4m3_rn_satfinite(fl32(w[n,k] / ws[n/128, k/128]))
+ * w : fp32 or bf16 (wtype) [N][K] row-major, 16-byte aligned.
+ * wq: u8 [N][K], 16-byte aligned.  ws: fp32 [ceil(N/128)][K/128].
+ * N >= 1 (a ragged last block is allowed), K >= 128, K % 128 == 0.
+ */
+FP8BS_API fp8bs_status fp8_quant_weight_blocks(const void *w, fp8bs_dtype wtype, int N, int K,
+                                     uint8_t *wq, float *ws, void *stream);
+
+/*
+ * Bytes of device workspace the GEMM entry points need for this shape on the
+ * current device (it depends on the SM count).  Writes *bytes; on error
+ * writes 0.  The same answer serves fp8_blockscaled_gemm and
+ * fp8_blockscaled_gemm_fused; bf16_gemm_ref has its own query.
+ *
+ * Workspace contract: zero-fill it once (e.g. cudaMemsetAsync) before its
+ * first use.  Every call that completes leaves its counter words zero again,
+ * so one workspace serves any number of later calls and CUDA-graph replays.
+ * Calls that share a workspace must not run concurrently (same stream, or
+ * ordered by events).  After FP8BS_ERR_DEVICE_TIMEOUT, zero-fill it again.
+ */
+FP8BS_API fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, size_t *bytes);
+
+/*
+ * Block-scaled FP8 GEMM on pre-quantised operands [P1 "Why this shape is
+ * hard"]:
+ *   y[m*N + n] = bf16_rn( sum_kb s_a[m,kb] * s_w[n/128,kb]
+ *                          * sum_{k in kb} dec(aq[m,k]) * dec(wq[n,k]) )
+ * Swap-AB tcgen05 kernel (weights in the MMA M dimension, tokens in N),
+ * 128x128 weight tiles streamed by TMA, K split across every SM with a
+ * fixed-order reduction.
+ * aq: u8 [M][K], 16-byte aligned.   as: fp32 [M][K/128].
+ * wq: u8 [N][K], 16-byte aligned.   ws: fp32 [ceil(N/128)][K/128].
+ * y : bf16 [M][N], 2-byte aligned.
+ * 1 <= M <= 64, N >= 1, K >= 128, K % 128 == 0.
+ * workspace: device, 256-byte aligned, >= fp8_blockscaled_gemm_workspace_size.
+ * flags: 0 or FP8BS_FLAG_OVERLAP_PREV.
+ */
+FP8BS_API fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as,
+                                  const uint8_t *wq, const float *ws,
+                                  void *y, int M, int N, int K,
+                                  void *workspace, size_t workspace_bytes,
+                                  unsigned flags, void *stream);
+
+/*
+ * The whole layer from bf16 activations: activation quantisation (as
+ * fp8_quant_act) fused with the GEMM (as fp8_blockscaled_gemm).  The
+ * quantised activations are formed inside the GEMM kernel, per 128-wide K
+ * block, straight into shared memory in the tensor-core operand layout; they
+ * never reach global memory.  Bitwise identical to fp8_quant_act followed by
+ * fp8_blockscaled_gemm on the same inputs.
+ * x: bf16, M rows, row stride ldx elements, 16-byte aligned, ldx % 8 == 0.
+ * Other arguments as fp8_blockscaled_gemm.
+ */
+FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx,
+                                        const uint8_t *wq, const float *ws,
+                                        void *y, int M, int N, int K,
+                                        void *workspace, size_t workspace_bytes,
+                                        unsigned flags, void *stream);
+
+/*
+ * 16-bit comparison GEMM for the output layer [P2 "The output layer, which
+ * did run": the layer "still 16-bit" before conversion]:
+ *   y[m*N + n] = bf16_rn( sum_k x[m,k] * w[n,k] )   (fp32 accumulation)
+ * Same swap-AB / TMA / split-K pipeline with bf16 tensor-core MMAs and no
+ * block scales.
+ * x: bf16 [M][K], w: bf16 [N][K], both 16-byte aligned; y: bf16 [M][N].
+ * 1 <= M <= 64, N >= 1, K >= 64, K % 64 == 0.
+ */
+FP8BS_API fp8bs_status bf16_gemm_ref_workspace_size(int M, int N, int K, size_t *bytes);
+FP8BS_API fp8bs_status bf16_gemm_ref(const void *x, const void *w, void *y,
+                           int M, int N, int K,
+                           void *workspace, size_t workspace_bytes,
+                           unsigned flags, void *stream);
+
+/*
+ * Device-side failure report.  Every wait inside the GEMM kernels is bounded
+ * (about one second); a kernel that gives up records a code in the first
+ * word of its workspace, releases its tensor memory and returns.  This call
+ * synchronises the device, copies that word to *code (0 = none) and, when
+ * clear != 0, resets it.  Returns FP8BS_ERR_DEVICE_TIMEOUT when the word is
+ * non-zero, FP8BS_OK otherwise.
+ */
+FP8BS_API fp8bs_status fp8bs_workspace_status(const void *workspace, int clear, int *code);
+
+/*
+ * The K-split schedule the GEMMs use, exposed for inspection and tests.
+ * Work unit = (128-row weight tile, 128-wide K block) [(tile, 64-wide K
+ * block) for bf16_gemm_ref, bf16 = 1]; units are ordered tile-major and
+ * split into `ctas` contiguous ranges of equal size +-1, one per SM (fewer
+ * when there are fewer units).  num_sms <= 0 means "the current device".
+ * Writes the CTA count, the unit count and, for CTA `cta` (when >= 0), its
+ * first unit and one-past-last unit.
+ */
+FP8BS_API fp8bs_status fp8bs_split_plan(int N, int K, int bf16, int num_sms, int cta,
+                              int *ctas, long long *units,
+                              long long *unit_begin, long long *unit_end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

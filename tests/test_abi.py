@@ -1,0 +1,128 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every symbol the
+headers declare, and rejects bad arguments on the host before anything would
+reach a GPU.  Nothing here launches a kernel."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import fp8_block_scaled_token_gb300 as fb
+from fp8_block_scaled_token_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, SHAPE, MISALIGNED, WS_SMALL, DEVICE, CUDA, TIMEOUT = range(8)
+
+
+@pytest.fixture(scope="module")
+def L():
+    fbuild.build()
+    return fb.lib()
+
+
+def declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"FP8BS_API\s+[A-Za-z_][A-Za-z0-9_ ]*?\**\s*\b([a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_headers_declare_the_boundary():
+    names = declared_symbols()
+    for n in ("fp8_quant_act", "fp8_quant_weight_blocks", "fp8_blockscaled_gemm",
+              "fp8_blockscaled_gemm_fused", "fp8_blockscaled_gemm_workspace_size",
+              "bf16_gemm_ref", "bf16_gemm_ref_workspace_size", "fp8bs_status_string",
+              "fp8bs_workspace_status", "fp8bs_split_plan"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert names
+    raw = ctypes.CDLL(fb.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(L):
+    seen = set()
+    for code in range(8):
+        s = fb.status_string(code)
+        assert s and s not in seen
+        seen.add(s)
+    assert fb.status_string(99) == "unknown status"
+
+
+P = ctypes.c_void_p
+A16 = P(0x10000)      # 16-byte aligned fake address: never dereferenced
+A1 = P(0x10001)       # misaligned fake address
+NUL = P(0)
+S = P(0)              # default stream
+
+
+def test_quant_act_validation(L):
+    assert L.fp8_quant_act(NUL, 8, 512, 512, A16, A16, 0, S) == INVALID
+    assert L.fp8_quant_act(A16, 0, 512, 512, A16, A16, 0, S) == INVALID
+    assert L.fp8_quant_act(A16, 8, 512, 256, A16, A16, 0, S) == INVALID        # ldx < K
+    assert L.fp8_quant_act(A16, 8, 512, 512, A16, A16, 2, S) == INVALID        # unknown flag
+    assert L.fp8_quant_act(A16, 8, 500, 512, A16, A16, 0, S) == SHAPE          # K % 128
+    assert L.fp8_quant_act(A1, 8, 512, 512, A16, A16, 0, S) == MISALIGNED
+    assert L.fp8_quant_act(A16, 8, 512, 516, A16, A16, 0, S) == MISALIGNED     # ldx % 8
+
+
+def test_quant_weight_validation(L):
+    assert L.fp8_quant_weight_blocks(NUL, 0, 256, 512, A16, A16, S) == INVALID
+    assert L.fp8_quant_weight_blocks(A16, 7, 256, 512, A16, A16, S) == INVALID
+    assert L.fp8_quant_weight_blocks(A16, 0, 0, 512, A16, A16, S) == INVALID
+    assert L.fp8_quant_weight_blocks(A16, 0, 256, 200, A16, A16, S) == SHAPE
+    assert L.fp8_quant_weight_blocks(A16, 0, 256, 512, A1, A16, S) == MISALIGNED
+
+
+def test_gemm_validation(L):
+    g = L.fp8_blockscaled_gemm
+    assert g(NUL, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == INVALID
+    assert g(A16, A16, A16, A16, A16, 0, 256, 512, A16, 1 << 20, 0, S) == INVALID
+    assert g(A16, A16, A16, A16, A16, 65, 256, 512, A16, 1 << 20, 0, S) == SHAPE
+    assert g(A16, A16, A16, A16, A16, 8, 256, 520, A16, 1 << 20, 0, S) == SHAPE
+    assert g(A16, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 4, S) == INVALID
+    assert g(A1, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == MISALIGNED
+    assert g(A16, A16, A16, A16, A16, 8, 256, 512, P(0x10010), 1 << 20, 0, S) == MISALIGNED  # workspace % 256
+    f = L.fp8_blockscaled_gemm_fused
+    assert f(A16, 100, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == INVALID           # ldx < K
+    assert f(A16, 516, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == MISALIGNED        # ldx % 8
+    b = L.bf16_gemm_ref
+    assert b(A16, A16, A16, 8, 256, 96, A16, 1 << 20, 0, S) == SHAPE                         # K % 64
+    assert b(A16, A16, A16, 64, 256, 128, A16, 1 << 20, 0, S) != SHAPE
+    sz = ctypes.c_size_t(5)
+    assert L.fp8_blockscaled_gemm_workspace_size(8, 256, 100, ctypes.byref(sz)) == SHAPE and sz.value == 0
+
+
+def test_split_plan_partitions_units(L):
+    for (N, K, bf16, sms) in ((256, 512, 0, 152), (5120, 5120, 0, 152), (248320, 5120, 0, 152),
+                              (34816, 5120, 0, 148), (5120, 17408, 0, 160), (300, 640, 1, 152), (128, 128, 0, 1)):
+        ctas, units, _, _ = fb.split_plan(N, K, bool(bf16), sms)
+        kg = K // (64 if bf16 else 128)
+        assert units == ((N + 127) // 128) * kg
+        assert ctas == min(units, sms)
+        prev_end, sizes = 0, []
+        partial_tiles = {}
+        for c in range(ctas):
+            _, _, b, e = fb.split_plan(N, K, bool(bf16), sms, c)
+            assert b == prev_end and e > b
+            sizes.append(e - b)
+            prev_end = e
+            tiles = set(range(b // kg, (e - 1) // kg + 1))
+            owned = [t for t in tiles if b <= t * kg and (t + 1) * kg <= e]
+            partial_tiles[c] = sorted(tiles - set(owned))
+        assert prev_end == units
+        assert max(sizes) - min(sizes) <= 1
+        # the reduction gives every CTA two partial slots: it may never need more
+        assert all(len(v) <= 2 for v in partial_tiles.values())
+        # each split tile is shared by CTAs with consecutive indices
+        for t in range((N + 127) // 128):
+            contrib = [c for c, v in partial_tiles.items() if t in v]
+            if contrib:
+                assert contrib == list(range(contrib[0], contrib[-1] + 1))
