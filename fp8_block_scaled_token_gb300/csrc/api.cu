@@ -6,7 +6,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/fp8bs_testing.h"
+#include "fp8bs_testing.h"
 #include "internal.h"
 #include "plan.cuh"
 

@@ -19,8 +19,8 @@
 //               s_w[tile,kb] * s_a[m,kb] and adds into fp32 registers; at the
 //               end of a tile it stores bf16 Y, or hands its partial to the
 //               fixed-order K-split reduction.
-//   warps 6-9   (fused variant only) activation quantisation: each warp takes
-//               every 4th unit, reads the bf16 token rows of that K block,
+//   warps 6+    (fused variant only) activation quantisation: 2 or 4 warps,
+//               each taking every 2nd/4th unit, read the bf16 token rows of that K block,
 //               computes the per-token scale and writes E4M3 codes straight
 //               into the swizzled B-operand tile of the ring stage.
 //
@@ -33,6 +33,14 @@
 #include "plan.cuh"
 #include "ptx.cuh"
 #include "quant_math.cuh"
+
+// Shared-memory ring size (KB) and L2 prefetch depth (units); tuning knobs.
+#ifndef FP8BS_RING_KB
+#define FP8BS_RING_KB 100
+#endif
+#ifndef FP8BS_PREFETCH_UNITS
+#define FP8BS_PREFETCH_UNITS 16
+#endif
 
 namespace fp8bs {
 
@@ -69,11 +77,22 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kWBytes = kTileRows * kRowBytes;   // 16 KB
     static constexpr int kBBytes = NPAD * kRowBytes;        // 2..8 KB
     static constexpr int kStageBytes = kWBytes + kBBytes;   // multiple of 1024
-    static constexpr int kStages = (200 * 1024) / kStageBytes > 12 ? 12 : (200 * 1024) / kStageBytes;
+    // Two CTAs per SM where registers allow: about 100 KB of ring, so that a
+    // CTA of the next GEMM (launched early with programmatic dependent
+    // launch) fits on the same SM and starts streaming while this one
+    // drains.  The fused kernel at NPAD > 32 needs more registers per thread
+    // than two CTAs leave, so it keeps one CTA per SM and a 200 KB ring.
+    // L2 prefetches keep further tiles in flight beyond the ring.
+    static constexpr int kMinBlocks = ((MODE == kModeFp8Fused && NPAD > 32) || FP8BS_RING_KB > 110) ? 1 : 2;
+    static constexpr int kRingBudget = kMinBlocks == 2 ? FP8BS_RING_KB * 1024 : 200 * 1024;
+    static constexpr int kStages = kRingBudget / kStageBytes > 12 ? 12 : kRingBudget / kStageBytes;
+    static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;  // units prefetched into L2 ahead of the ring
     static constexpr int kAcc = 4;
     static constexpr int kTmemNeed = kAcc * NPAD;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
-    static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
+    // Quantisation warps of the fused kernel: two suffice up to 32 tokens
+    // (and keep the CTA small enough for two per SM), four above.
+    static constexpr int kQuantWarps = MODE != kModeFp8Fused ? 0 : (NPAD > 32 ? 4 : 2);
     static constexpr int kEpiWarps = 4;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kSaOffset = kStages * kStageBytes;
@@ -85,12 +104,12 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr uint32_t kIdesc =
         MODE == kModeBf16 ? idesc_bf16_f32(kTileRows, NPAD) : idesc_e4m3_f32(kTileRows, NPAD);
     static_assert(kStageBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-    static_assert(kStages >= 5, "the fused quant warps rely on a ring of at least 5 stages");
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    static_assert(kStages >= kQuantWarps, "the fused quant warps rely on a ring of at least kQuantWarps stages");
+    static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "shared memory per SM");
 };
 
 template <int NPAD, int MODE>
-__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, MODE>::kMinBlocks)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p)
 {
@@ -166,6 +185,20 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
             const uint32_t tx = C::kWBytes + (MODE == kModeFp8Fused ? 0 : C::kBBytes);
             uint32_t armed_mask = 0, armed_parity = 0;
             const int pre = p.prefetch_before_wait ? (nunits < C::kStages ? nunits : C::kStages) : 0;
+            // Units beyond the first ring pass go to L2 ahead of time (once the
+            // weights may be read: before the dependency wait only with the
+            // overlap flag).
+            int prefetched = C::kStages;
+            bool weights_readable = p.prefetch_before_wait != 0;
+            auto prefetch_upto = [&](int limit) {
+                if (!weights_readable)
+                    return;
+                for (; prefetched < limit && prefetched < nunits; ++prefetched) {
+                    const long long u = u0 + prefetched;
+                    tma_prefetch_l2_2d(&tm_w, static_cast<int>(u % kg) * C::kChunkElems,
+                                       static_cast<int>(u / kg) * C::kTileRows);
+                }
+            };
             // Weights for the first ring pass, possibly before the previous grid is done.
             for (int i = 0; i < pre; ++i) {
                 if (i == p.test_skip_unit)
@@ -177,7 +210,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                 tma_load_2d(smem + i * C::kStageBytes, &tm_w, &full[i], kb * C::kChunkElems,
                             tile * C::kTileRows, pol_w);
             }
+            prefetch_upto(pre + C::kPrefetch);
             grid_dependency_wait();
+            weights_readable = true;  // the previous grid has completed
             if (MODE != kModeFp8Fused) {
                 for (int i = 0; i < pre; ++i) {
                     if (i == p.test_skip_unit)
@@ -204,6 +239,10 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                 if (MODE != kModeFp8Fused)
                     tma_load_2d(smem + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems, 0,
                                 pol_b);
+                // keep the L2 prefetch kPrefetch units ahead of the ring, once
+                // the first ring pass has been requested
+                if (i + 1 >= C::kStages)
+                    prefetch_upto(i + 1 + C::kPrefetch);
             }
             // Nothing may still be landing in shared memory when the CTA exits:
             // wait (bounded) for the last phase armed on every stage.
@@ -360,6 +399,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                             p.y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
                 }
             } else {
+                // K-split tile: publish this CTA's partial, and the last
+                // contributor to arrive sums all of them in contributor order.
                 const long long t_first = static_cast<long long>(tile) * kg;
                 const int c_first = plan_owner(p.units, p.ctas, t_first);
                 const int c_last = plan_owner(p.units, p.ctas, t_first + kg - 1);
@@ -367,28 +408,50 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
 #pragma unroll
                 for (int m = 0; m < NPAD; ++m)
                     if (m < p.M)
-                        mine[m * 128 + row] = acc[m];
-                __threadfence();
+                        __stcg(mine + m * 128 + row, acc[m]);
                 named_bar_sync(1, 32 * C::kEpiWarps);
                 if (warp == 2 && lane == 0) {
-                    const unsigned prev = atomicAdd(&p.counters[tile], 1u);
+                    // one release for the whole epilogue group's stores (ordered
+                    // by the barrier above); acquire for the others' partials
+                    const unsigned prev = atomic_add_acq_rel_gpu(&p.counters[tile], 1u);
                     *last_flag = (prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
                 }
                 named_bar_sync(1, 32 * C::kEpiWarps);
                 if (*last_flag) {
-                    // Sum every contributor's slot (this CTA's included) in
-                    // contributor order, whatever the arrival order was.
-                    __threadfence();
 #pragma unroll
                     for (int m = 0; m < NPAD; ++m)
                         acc[m] = 0.0f;
-                    for (int c = c_first; c <= c_last; ++c) {
-                        const float *src =
-                            p.slots + static_cast<long long>(plan_slot(p.units, p.ctas, kg, c, tile)) * (NPAD * 128);
+                    // Issue every contributor's loads for a chunk of tokens at
+                    // once (one L2 round trip per chunk), then add them in
+                    // contributor order.
+                    constexpr int kMaxC = 6;
+                    constexpr int kMC = NPAD <= 16 ? 16 : 8;
+                    for (int c0 = c_first; c0 <= c_last; c0 += kMaxC) {
+                        const int nc = c_last - c0 + 1 < kMaxC ? c_last - c0 + 1 : kMaxC;
+                        const float *src[kMaxC];
 #pragma unroll
-                        for (int m = 0; m < NPAD; ++m)
-                            if (m < p.M)
-                                acc[m] += __ldcg(src + m * 128 + row);
+                        for (int j = 0; j < kMaxC; ++j)
+                            src[j] = p.slots +
+                                     static_cast<long long>(plan_slot(p.units, p.ctas, kg, c0 + (j < nc ? j : 0), tile)) *
+                                         (NPAD * 128) +
+                                     row;
+#pragma unroll
+                        for (int mc = 0; mc < NPAD; mc += kMC) {
+                            if (mc >= p.M)
+                                break;
+                            float v[kMaxC][kMC];
+#pragma unroll
+                            for (int j = 0; j < kMaxC; ++j)
+#pragma unroll
+                                for (int q = 0; q < kMC; ++q)
+                                    v[j][q] = (j < nc && mc + q < p.M) ? __ldcg(src[j] + (mc + q) * 128) : 0.0f;
+#pragma unroll
+                            for (int j = 0; j < kMaxC; ++j)
+#pragma unroll
+                                for (int q = 0; q < kMC; ++q)
+                                    if (j < nc)
+                                        acc[mc + q] += v[j][q];
+                        }
                     }
                     if (n < p.N) {
 #pragma unroll
@@ -419,26 +482,44 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                 const int kb = static_cast<int>((u0 + i) % kg);
                 const uint16_t *xk = p.x + static_cast<long long>(kb) * 128 + lane * 4;
                 uint8_t *btile = smem + s * C::kStageBytes + C::kWBytes;
+                // Eight token rows at a time, interleaved so their loads,
+                // reductions and divisions overlap.
                 for (int m0 = 0; m0 < p.M; m0 += 8) {
                     uint2 raw[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        if (m0 + j < p.M)
-                            raw[j] = *reinterpret_cast<const uint2 *>(xk + static_cast<long long>(m0 + j) * p.ldx);
+                        raw[j] = (m0 + j < p.M)
+                                     ? *reinterpret_cast<const uint2 *>(xk + static_cast<long long>(m0 + j) * p.ldx)
+                                     : make_uint2(0u, 0u);
+                    float v[8][4], am[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[j][0] = bf16_lo(raw[j].x);
+                        v[j][1] = bf16_hi(raw[j].x);
+                        v[j][2] = bf16_lo(raw[j].y);
+                        v[j][3] = bf16_hi(raw[j].y);
+                        am[j] = abs_max4(v[j][0], v[j][1], v[j][2], v[j][3]);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int m = m0 + j;
-                        if (m < p.M) {
-                            uint32_t codes;
-                            const float sc = quant_group_warp(raw[j], codes);
-                            // row m, bytes 4*lane..4*lane+3 of the 128-byte row; the 16-byte
-                            // chunk index is XOR-ed with (row mod 8) as TMA's 128-byte swizzle does.
-                            const uint32_t off =
-                                static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) + ((lane & 3) << 2));
-                            *reinterpret_cast<uint32_t *>(btile + off) = codes;
-                            if (lane == 0)
-                                sa_ring[s * 64 + m] = sc;
-                        }
+                        if (m >= p.M)
+                            break; // warp-uniform; rows >= M stay zero
+                        const float sc = group_scale(am[j]);
+                        const uint32_t codes = quantize4(v[j][0], v[j][1], v[j][2], v[j][3], sc);
+                        // row m, bytes 4*lane..4*lane+3 of its 128-byte row; the
+                        // 16-byte chunk index is XOR-ed with (row mod 8) as TMA's
+                        // 128-byte swizzle does.
+                        const uint32_t off =
+                            static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) + ((lane & 3) << 2));
+                        *reinterpret_cast<uint32_t *>(btile + off) = codes;
+                        if (lane == 0)
+                            sa_ring[s * 64 + m] = sc;
                     }
                 }
                 fence_proxy_async_smem();

@@ -7,7 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
-#include "../../include/fp8bs.h"
+#include "fp8bs.h"
 
 namespace fp8bs {
 

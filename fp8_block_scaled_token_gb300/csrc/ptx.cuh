@@ -132,6 +132,27 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// Bring a 2-D tile into L2 only (no shared memory, no completion tracking):
+// lets the producer keep many more bytes in flight than its ring holds.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// ------------------------------------------------------- global atomics
+// Device-scope add with acquire-release semantics: releases every write
+// that happens-before it (including other threads' writes ordered by a
+// preceding CTA barrier) and acquires the writes released by earlier adds.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // ----------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void grid_dependency_wait()
 {

@@ -1,0 +1,51 @@
+"""Host-side logic of bench.py on the CPU: the multi-rank timing aggregation
+(barrier + max over ranks, whole-job throughput) with two gloo ranks, and the
+byte accounting of the roofline."""
+import os
+import socket
+
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    t = bench.max_over_ranks(1.0 + rank, world)          # rank 1 is the slow one
+    v = bench.whole_job_value(1e9, 10, world, t)
+    q.put((rank, t, v))
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t, v in out:
+        assert t == 2.0                        # max over ranks, seen by every rank
+        assert abs(v - 1e9 * 10 * 2 / 2.0 / 1e9) < 1e-9
+
+
+def test_algorithmic_bytes():
+    # square decode layer, M=8: Wq + s_w + X bf16 + Y bf16
+    assert bench.algorithmic_bytes(8, 5120, 5120) == 26214400 + 6400 + 81920 + 81920
+    # vocab layer, M=8
+    assert bench.algorithmic_bytes(8, 248320, 5120) == 1271398400 + 310400 + 81920 + 3973120
+    assert bench.bf16_bytes(8, 248320, 5120) == 2542796800 + 81920 + 3973120
+    assert bench.whole_job_value(26384640, 1000, 1, 0.005) == 26384640 * 1000 / 0.005 / 1e9
