@@ -275,7 +275,7 @@ def run_ours(args, world, rank, local):
     wqs, wss = [], []
     for i in range(R):
         w = synth.weights(N, K, seed=100 + i, outlier_p=cfg.get("w_outlier_p", 0.0), device=dev)
-        wq, ws = fb.fp8_quant_weight_blocks(w)
+        wq, ws = fb.fp8_quant_weight_blocks(w, tiled=True)
         wqs.append(wq)
         wss.append(ws)
         del w
@@ -286,7 +286,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
 
     def step(i):
-        fb.fp8_blockscaled_gemm_fused(x, wqs[i % R], wss[i % R], y=y, workspace=work, flags=flags)
+        fb.fp8_blockscaled_gemm_fused(x, wqs[i % R], wss[i % R], y=y, workspace=work, flags=flags, n=N)
 
     # warm-up (eager), then capture one ring pass and the remainder as graphs
     for i in range(args.warmup):
@@ -357,14 +357,14 @@ def run_ours(args, world, rank, local):
     e2e_steps = min(steps, 5000)
     for i in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        fb.fp8_blockscaled_gemm_fused(x_dev, wqs[i % R], wss[i % R], y=y, workspace=work)
+        fb.fp8_blockscaled_gemm_fused(x_dev, wqs[i % R], wss[i % R], y=y, workspace=work, n=N)
         y_host.copy_(y, non_blocking=True)
     torch.cuda.synchronize()
     barrier(world)
     start.record()
     for i in range(e2e_steps):
         x_dev.copy_(x_host, non_blocking=True)
-        fb.fp8_blockscaled_gemm_fused(x_dev, wqs[i % R], wss[i % R], y=y, workspace=work)
+        fb.fp8_blockscaled_gemm_fused(x_dev, wqs[i % R], wss[i % R], y=y, workspace=work, n=N)
         y_host.copy_(y, non_blocking=True)
     end.record()
     torch.cuda.synchronize()
@@ -379,7 +379,7 @@ def run_ours(args, world, rank, local):
 
     def step2(i):
         fb.fp8_quant_act(x, xq=xq, xs=xs, flags=flags)
-        fb.fp8_blockscaled_gemm(xq, xs, wqs[i % R], wss[i % R], y=y, workspace=work, flags=flags)
+        fb.fp8_blockscaled_gemm(xq, xs, wqs[i % R], wss[i % R], y=y, workspace=work, flags=flags, n=N)
 
     for i in range(20):
         step2(i)
@@ -414,6 +414,7 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
             "config": {"workload": "%s M=%d N=%d K=%d" % (args.workload, M, N, K), "M": M, "N": N, "K": K,
                        "kernel": "fp8_blockscaled_gemm_fused (cast fused, swap-AB tcgen05, split-K)",
+                       "weights": "E4M3 tiled layout (one contiguous 16 KB run per 128x128 tile)",
                        "weights_ring": R, "l2": "ring of %d distinct %.1f MB weight layers (%.0f MB) > 4x L2 (%.0f MB)" % (
                            R, layer_bytes / 1e6, R * layer_bytes / 1e6, l2 / 1e6),
                        "timing": "CUDA graphs of %d launches replayed; PDL between launches; CUDA events" % R,
@@ -475,16 +476,16 @@ def sweep(args, dev):
         layers = []
         for i in range(R):
             w = synth.weights(N, K, seed=200 + i, outlier_p=cfg.get("w_outlier_p", 0.0), device=dev)
-            layers.append(fb.fp8_quant_weight_blocks(w))
+            layers.append(fb.fp8_quant_weight_blocks(w, tiled=True))
             del w
         for M in Ms:
             x = synth.activations(M, K, seed=cfg["seed"], outlier_p=cfg.get("x_outlier_p", 0.0), device=dev)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K), dev)
 
-            def f(i, x=x, y=y, work=work):
+            def f(i, x=x, y=y, work=work, N=N):
                 wq, ws = layers[i % R]
-                fb.fp8_blockscaled_gemm_fused(x, wq, ws, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV)
+                fb.fp8_blockscaled_gemm_fused(x, wq, ws, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
             us = time_graph(f, R, max(1, 400 // R), stream)
             b = algorithmic_bytes(M, N, K)
             out.append({"workload": name, "M": M, "N": N, "K": K, "us": round(us, 3),
@@ -495,14 +496,15 @@ def sweep(args, dev):
     # vocab layer in bf16 (the 16-bit baseline of the output layer)
     cfg = workload("vocab")
     N, K = cfg["N"], cfg["K"]
-    wb = [synth.weights(N, K, seed=300 + i, device=dev).to(torch.bfloat16) for i in range(2)]
+    wb = [fb.bf16_pack_weights_tiled(synth.weights(N, K, seed=300 + i, device=dev).to(torch.bfloat16))
+          for i in range(2)]
     for M in (1, 8):
         x = synth.activations(M, K, seed=4, device=dev)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         work = fb.make_workspace(fb.bf16_gemm_ref_workspace_size(M, N, K), dev)
 
         def f(i, x=x, y=y, work=work):
-            fb.bf16_gemm_ref(x, wb[i % 2], y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV)
+            fb.bf16_gemm_ref(x, wb[i % 2], y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
         us = time_graph(f, 2, 50, stream)
         b = bf16_bytes(M, N, K)
         out.append({"workload": "vocab_bf16", "M": M, "N": N, "K": K, "us": round(us, 3),

@@ -21,6 +21,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "lib", "libfp8bs.so")
 
 FLAG_OVERLAP_PREV = 1
+FLAG_WEIGHTS_TILED = 2
 F32, BF16 = 0, 1
 
 _lib = None
@@ -47,6 +48,8 @@ def lib():
     sigs = {
         "fp8_quant_act": [vp, i, i, i, vp, vp, u, vp],
         "fp8_quant_weight_blocks": [vp, i, i, i, vp, vp, vp],
+        "fp8_quant_weight_blocks_tiled": [vp, i, i, i, vp, vp, vp],
+        "bf16_pack_weights_tiled": [vp, i, i, vp, vp],
         "fp8_blockscaled_gemm_workspace_size": [i, i, i, ctypes.POINTER(sz)],
         "fp8_blockscaled_gemm": [vp, vp, vp, vp, vp, i, i, i, vp, sz, u, vp],
         "fp8_blockscaled_gemm_fused": [vp, i, vp, vp, vp, i, i, i, vp, sz, u, vp],
@@ -121,8 +124,12 @@ def fp8_quant_act(x, xq=None, xs=None, flags=0):
     return xq, xs
 
 
-def fp8_quant_weight_blocks(w, wq=None, ws=None):
-    """fp32 or bf16 W [N, K] -> (wq uint8 [N,K], ws fp32 [ceil(N/128), K/128])."""
+def fp8_quant_weight_blocks(w, wq=None, ws=None, tiled=False):
+    """fp32 or bf16 W [N, K] -> (wq, ws fp32 [ceil(N/128), K/128]).
+
+    wq is uint8 [N, K] row-major, or with ``tiled=True`` uint8
+    [ceil(N/128) * K/128, 128, 128]: one contiguous 128x128 block per weight
+    tile (rows past N zero), for the GEMMs' tiled-weight mode."""
     torch = _torch()
     if w.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("w must be float32 or bfloat16")
@@ -131,12 +138,43 @@ def fp8_quant_weight_blocks(w, wq=None, ws=None):
         raise ValueError("w must be contiguous")
     N, K = w.shape
     if wq is None:
-        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+        shape = (((N + 127) // 128) * max(K // 128, 0), 128, 128) if tiled else (N, K)
+        wq = torch.empty(shape, dtype=torch.uint8, device=w.device)
     if ws is None:
         ws = torch.empty(((N + 127) // 128, max(K // 128, 0)), dtype=torch.float32, device=w.device)
     wt = BF16 if w.dtype == torch.bfloat16 else F32
-    _check("fp8_quant_weight_blocks", lib().fp8_quant_weight_blocks(_ptr(w), wt, N, K, _ptr(wq), _ptr(ws), _stream()))
+    fn = lib().fp8_quant_weight_blocks_tiled if tiled else lib().fp8_quant_weight_blocks
+    _check("fp8_quant_weight_blocks", fn(_ptr(w), wt, N, K, _ptr(wq), _ptr(ws), _stream()))
     return wq, ws
+
+
+def bf16_pack_weights_tiled(w, wt=None):
+    """bf16 W [N, K] -> bf16 [ceil(N/128) * K/64, 128, 64], one contiguous
+    128x64 tile per block (rows past N zero), for bf16_gemm_ref(tiled)."""
+    torch = _torch()
+    _need(w, torch.bfloat16, "w")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    N, K = w.shape
+    if wt is None:
+        wt = torch.empty((((N + 127) // 128) * max(K // 64, 0), 128, 64), dtype=torch.bfloat16, device=w.device)
+    _check("bf16_pack_weights_tiled", lib().bf16_pack_weights_tiled(_ptr(w), N, K, _ptr(wt), _stream()))
+    return wt
+
+
+def _weight_dims(wq, K, n, what):
+    """(N, flag) of a row-major [N,K] or tiled [tiles,128,*] weight operand."""
+    if wq.dim() == 2:
+        if wq.shape[1] != K:
+            raise ValueError("operand shapes do not agree")
+        return wq.shape[0], 0
+    if wq.dim() == 3 and wq.shape[1] == 128:
+        if n is None:
+            raise ValueError("%s is tiled: pass n= (the number of weight rows)" % what)
+        if wq.numel() != ((int(n) + 127) // 128) * 128 * K:
+            raise ValueError("tiled %s does not hold ceil(n/128)*128*K elements" % what)
+        return int(n), FLAG_WEIGHTS_TILED
+    raise ValueError("%s must be [N, K] or tiled [tiles, 128, *]" % what)
 
 
 def fp8_blockscaled_gemm_workspace_size(M, N, K):
@@ -157,19 +195,21 @@ def make_workspace(nbytes, device=None):
     return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
 
 
-def fp8_blockscaled_gemm(aq, as_, wq, ws, y=None, workspace=None, flags=0):
-    """Y[M,N] bf16 from pre-quantised operands."""
+def fp8_blockscaled_gemm(aq, as_, wq, ws, y=None, workspace=None, flags=0, n=None):
+    """Y[M,N] bf16 from pre-quantised operands (wq row-major, or tiled with
+    n= the number of weight rows)."""
     torch = _torch()
     _need(aq, torch.uint8, "aq")
     _need(as_, torch.float32, "as_")
-    _need(wq, torch.uint8, "wq")
+    _need(wq, torch.uint8, "wq", ndim=wq.dim() if wq.dim() in (2, 3) else 2)
     _need(ws, torch.float32, "ws")
-    for t, n in ((aq, "aq"), (as_, "as_"), (wq, "wq"), (ws, "ws")):
+    for t, nm in ((aq, "aq"), (as_, "as_"), (wq, "wq"), (ws, "ws")):
         if not t.is_contiguous():
-            raise ValueError("%s must be contiguous" % n)
+            raise ValueError("%s must be contiguous" % nm)
     M, K = aq.shape
-    N = wq.shape[0]
-    if wq.shape[1] != K or tuple(as_.shape) != (M, K // 128) or tuple(ws.shape) != ((N + 127) // 128, K // 128):
+    N, tf = _weight_dims(wq, K, n, "wq")
+    flags |= tf
+    if tuple(as_.shape) != (M, K // 128) or tuple(ws.shape) != ((N + 127) // 128, K // 128):
         raise ValueError("operand shapes do not agree")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
@@ -181,16 +221,18 @@ def fp8_blockscaled_gemm(aq, as_, wq, ws, y=None, workspace=None, flags=0):
     return y
 
 
-def fp8_blockscaled_gemm_fused(x, wq, ws, y=None, workspace=None, flags=0):
-    """Y[M,N] bf16 from bf16 activations (row stride may exceed K)."""
+def fp8_blockscaled_gemm_fused(x, wq, ws, y=None, workspace=None, flags=0, n=None):
+    """Y[M,N] bf16 from bf16 activations (row stride may exceed K); wq
+    row-major, or tiled with n= the number of weight rows."""
     torch = _torch()
     _need(x, torch.bfloat16, "x")
     _rows_contiguous(x, "x")
-    _need(wq, torch.uint8, "wq")
+    _need(wq, torch.uint8, "wq", ndim=wq.dim() if wq.dim() in (2, 3) else 2)
     _need(ws, torch.float32, "ws")
     M, K = x.shape
-    N = wq.shape[0]
-    if wq.shape[1] != K or tuple(ws.shape) != ((N + 127) // 128, K // 128):
+    N, tf = _weight_dims(wq, K, n, "wq")
+    flags |= tf
+    if tuple(ws.shape) != ((N + 127) // 128, K // 128):
         raise ValueError("operand shapes do not agree")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
@@ -202,17 +244,17 @@ def fp8_blockscaled_gemm_fused(x, wq, ws, y=None, workspace=None, flags=0):
     return y
 
 
-def bf16_gemm_ref(x, w, y=None, workspace=None, flags=0):
-    """Y[M,N] bf16 = X bf16 [M,K] . W bf16 [N,K]^T (fp32 accumulation)."""
+def bf16_gemm_ref(x, w, y=None, workspace=None, flags=0, n=None):
+    """Y[M,N] bf16 = X bf16 [M,K] . W bf16 [N,K]^T (fp32 accumulation); w
+    row-major, or tiled (bf16_pack_weights_tiled) with n= the weight rows."""
     torch = _torch()
     _need(x, torch.bfloat16, "x")
-    _need(w, torch.bfloat16, "w")
+    _need(w, torch.bfloat16, "w", ndim=w.dim() if w.dim() in (2, 3) else 2)
     if not (x.is_contiguous() and w.is_contiguous()):
         raise ValueError("x and w must be contiguous")
     M, K = x.shape
-    N = w.shape[0]
-    if w.shape[1] != K:
-        raise ValueError("operand shapes do not agree")
+    N, tf = _weight_dims(w, K, n, "w")
+    flags |= tf
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if workspace is None:

@@ -142,9 +142,28 @@ fp8bs_status check_gemm_shape(int M, int N, int K, int kmult)
     return FP8BS_OK;
 }
 
-fp8bs_status check_flags(unsigned flags)
+fp8bs_status check_flags(unsigned flags, unsigned allowed)
 {
-    return (flags & ~FP8BS_FLAG_OVERLAP_PREV) ? FP8BS_ERR_INVALID_ARG : FP8BS_OK;
+    return (flags & ~allowed) ? FP8BS_ERR_INVALID_ARG : FP8BS_OK;
+}
+
+constexpr unsigned kGemmFlags = FP8BS_FLAG_OVERLAP_PREV | FP8BS_FLAG_WEIGHTS_TILED;
+
+fp8bs_status quant_weight_common(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq, float *ws,
+                                 bool tiled, void *stream)
+{
+    if (!w || !wq || !ws || N < 1 || K < 1 || (wtype != FP8BS_F32 && wtype != FP8BS_BF16))
+        return FP8BS_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N > (1 << 30) || K > (1 << 30) ||
+        static_cast<long long>((N + 127) / 128) * (K / 128) > 0x7FFFFFFFll)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w, 16) || !aligned(wq, 16) || !aligned(ws, 4))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo dev;
+    fp8bs_status st = current_device(&dev);
+    if (st != FP8BS_OK)
+        return st;
+    return launch_quant_weight(w, wtype, N, K, wq, ws, tiled, static_cast<cudaStream_t>(stream));
 }
 
 fp8bs_status gemm_workspace(int mode, int M, int N, int K, size_t *bytes)
@@ -209,7 +228,7 @@ fp8bs_status fp8_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, fl
 {
     if (!x || !xq || !xs || M < 1 || K < 1 || ldx < K)
         return FP8BS_ERR_INVALID_ARG;
-    if (check_flags(flags) != FP8BS_OK)
+    if (check_flags(flags, FP8BS_FLAG_OVERLAP_PREV) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (K % 128 != 0 || K > (1 << 30) || static_cast<long long>(M) * (K / 128) > (1ll << 34))
         return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -226,18 +245,29 @@ fp8bs_status fp8_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, fl
 fp8bs_status fp8_quant_weight_blocks(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq, float *ws,
                                      void *stream)
 {
-    if (!w || !wq || !ws || N < 1 || K < 1 || (wtype != FP8BS_F32 && wtype != FP8BS_BF16))
+    return quant_weight_common(w, wtype, N, K, wq, ws, false, stream);
+}
+
+fp8bs_status fp8_quant_weight_blocks_tiled(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq,
+                                           float *ws, void *stream)
+{
+    return quant_weight_common(w, wtype, N, K, wq, ws, true, stream);
+}
+
+fp8bs_status bf16_pack_weights_tiled(const void *w, int N, int K, void *wt, void *stream)
+{
+    if (!w || !wt || N < 1 || K < 1)
         return FP8BS_ERR_INVALID_ARG;
-    if (K % 128 != 0 || N > (1 << 30) || K > (1 << 30) ||
-        static_cast<long long>((N + 127) / 128) * (K / 128) > 0x7FFFFFFFll)
+    if (K % 64 != 0 || N > (1 << 30) || K > (1 << 30) ||
+        static_cast<long long>((N + 127) / 128) * (K / 64) > 0x7FFFFFFFll)
         return FP8BS_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(w, 16) || !aligned(wq, 16) || !aligned(ws, 4))
+    if (!aligned(w, 16) || !aligned(wt, 16))
         return FP8BS_ERR_MISALIGNED;
     DeviceInfo dev;
     fp8bs_status st = current_device(&dev);
     if (st != FP8BS_OK)
         return st;
-    return launch_quant_weight(w, wtype, N, K, wq, ws, static_cast<cudaStream_t>(stream));
+    return launch_pack_bf16_tiled(w, N, K, wt, static_cast<cudaStream_t>(stream));
 }
 
 fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, size_t *bytes)
@@ -271,7 +301,7 @@ fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as, const uint
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
-    if (check_flags(flags) != FP8BS_OK)
+    if (check_flags(flags, kGemmFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(aq, 16) || !aligned(wq, 16) || !aligned(as, 4) || !aligned(ws, 4) || !aligned(y, 2) ||
         !aligned(workspace, 256))
@@ -305,7 +335,7 @@ fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx, const uint8_t *w
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
-    if (ldx < K || check_flags(flags) != FP8BS_OK)
+    if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||
         !aligned(workspace, 256))
@@ -337,7 +367,7 @@ fp8bs_status bf16_gemm_ref(const void *x, const void *w, void *y, int M, int N, 
     fp8bs_status st = check_gemm_shape(M, N, K, 64);
     if (st != FP8BS_OK)
         return st;
-    if (check_flags(flags) != FP8BS_OK)
+    if (check_flags(flags, kGemmFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 2) || !aligned(workspace, 256))
         return FP8BS_ERR_MISALIGNED;

@@ -36,10 +36,10 @@
 
 // Shared-memory ring size (KB) and L2 prefetch depth (units); tuning knobs.
 #ifndef FP8BS_RING_KB
-#define FP8BS_RING_KB 100
+#define FP8BS_RING_KB 200
 #endif
 #ifndef FP8BS_PREFETCH_UNITS
-#define FP8BS_PREFETCH_UNITS 16
+#define FP8BS_PREFETCH_UNITS 0
 #endif
 
 namespace fp8bs {
@@ -65,6 +65,7 @@ struct GemmParams {
     unsigned *counters;      // [ntiles] arrival counters, zero between calls
     float *slots;            // [2 * ctas][NPAD * 128] fp32 partials
     int prefetch_before_wait;// weights may be fetched before the previous grid completes
+    int w_tiled;             // weights in the tiled layout (one contiguous 16 KB run per tile)
     int test_skip_unit;      // -1, or a unit whose stage the producer never fills
     unsigned long long timeout_ns;
 };
@@ -77,14 +78,14 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kWBytes = kTileRows * kRowBytes;   // 16 KB
     static constexpr int kBBytes = NPAD * kRowBytes;        // 2..8 KB
     static constexpr int kStageBytes = kWBytes + kBBytes;   // multiple of 1024
-    // Two CTAs per SM where registers allow: about 100 KB of ring, so that a
-    // CTA of the next GEMM (launched early with programmatic dependent
-    // launch) fits on the same SM and starts streaming while this one
-    // drains.  The fused kernel at NPAD > 32 needs more registers per thread
-    // than two CTAs leave, so it keeps one CTA per SM and a 200 KB ring.
-    // L2 prefetches keep further tiles in flight beyond the ring.
+    // Ring size: HBM and cross-die L2 latencies on this part are long (over
+    // a microsecond under load), so one CTA per SM with a ~200 KB ring keeps
+    // the most bytes in flight.  A ring of <= 110 KB instead lets a CTA of
+    // the next GEMM (launched early with programmatic dependent launch) share
+    // the SM; the fused kernel at NPAD > 32 needs more registers than that
+    // leaves.  Optional L2 prefetches run further ahead of the ring.
     static constexpr int kMinBlocks = ((MODE == kModeFp8Fused && NPAD > 32) || FP8BS_RING_KB > 110) ? 1 : 2;
-    static constexpr int kRingBudget = kMinBlocks == 2 ? FP8BS_RING_KB * 1024 : 200 * 1024;
+    static constexpr int kRingBudget = (kMinBlocks == 2 ? FP8BS_RING_KB : (FP8BS_RING_KB > 110 ? FP8BS_RING_KB : 200)) * 1024;
     static constexpr int kStages = kRingBudget / kStageBytes > 12 ? 12 : kRingBudget / kStageBytes;
     static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;  // units prefetched into L2 ahead of the ring
     static constexpr int kAcc = 4;
@@ -92,7 +93,7 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
     // Quantisation warps of the fused kernel: two suffice up to 32 tokens
     // (and keep the CTA small enough for two per SM), four above.
-    static constexpr int kQuantWarps = MODE != kModeFp8Fused ? 0 : (NPAD > 32 ? 4 : 2);
+    static constexpr int kQuantWarps = MODE != kModeFp8Fused ? 0 : ((kMinBlocks == 2 && NPAD <= 32) ? 2 : 4);
     static constexpr int kEpiWarps = 4;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kSaOffset = kStages * kStageBytes;
@@ -133,6 +134,13 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     const long long u0 = plan_begin(p.units, p.ctas, cta);
     const int nunits = static_cast<int>(plan_begin(p.units, p.ctas, cta + 1) - u0);
     const int kg = p.kg;
+    // TMA coordinates of the weight tile of unit u: (K offset, row) in the
+    // row-major matrix, or (0, u*128) in the tiled layout where the tiles of
+    // consecutive units are consecutive 16 KB runs.
+    auto w_x = [&](long long u) { return p.w_tiled ? 0 : static_cast<int>(u % kg) * C::kChunkElems; };
+    auto w_y = [&](long long u) {
+        return p.w_tiled ? static_cast<int>(u * C::kTileRows) : static_cast<int>(u / kg) * C::kTileRows;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -195,8 +203,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     return;
                 for (; prefetched < limit && prefetched < nunits; ++prefetched) {
                     const long long u = u0 + prefetched;
-                    tma_prefetch_l2_2d(&tm_w, static_cast<int>(u % kg) * C::kChunkElems,
-                                       static_cast<int>(u / kg) * C::kTileRows);
+                    tma_prefetch_l2_2d(&tm_w, w_x(u), w_y(u));
                 }
             };
             // Weights for the first ring pass, possibly before the previous grid is done.
@@ -204,11 +211,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 if (i == p.test_skip_unit)
                     continue;
                 const long long u = u0 + i;
-                const int tile = static_cast<int>(u / kg), kb = static_cast<int>(u % kg);
                 mbar_arrive_expect_tx(&full[i], tx);
                 armed_mask |= 1u << i;
-                tma_load_2d(smem + i * C::kStageBytes, &tm_w, &full[i], kb * C::kChunkElems,
-                            tile * C::kTileRows, pol_w);
+                tma_load_2d(smem + i * C::kStageBytes, &tm_w, &full[i], w_x(u), w_y(u), pol_w);
             }
             prefetch_upto(pre + C::kPrefetch);
             grid_dependency_wait();
@@ -230,12 +235,11 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 if (i == p.test_skip_unit)
                     continue;
                 const long long u = u0 + i;
-                const int tile = static_cast<int>(u / kg), kb = static_cast<int>(u % kg);
+                const int kb = static_cast<int>(u % kg);
                 mbar_arrive_expect_tx(&full[s], tx);
                 armed_mask |= 1u << s;
                 armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
-                tma_load_2d(smem + s * C::kStageBytes, &tm_w, &full[s], kb * C::kChunkElems, tile * C::kTileRows,
-                            pol_w);
+                tma_load_2d(smem + s * C::kStageBytes, &tm_w, &full[s], w_x(u), w_y(u), pol_w);
                 if (MODE != kModeFp8Fused)
                     tma_load_2d(smem + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems, 0,
                                 pol_b);
@@ -482,6 +486,13 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const int kb = static_cast<int>((u0 + i) % kg);
                 const uint16_t *xk = p.x + static_cast<long long>(kb) * 128 + lane * 4;
                 uint8_t *btile = smem + s * C::kStageBytes + C::kWBytes;
+                // Pull the token rows of this warp's next unit into L1 now, so
+                // their loads do not wait a full L2 round trip later.
+                if (i + C::kQuantWarps < nunits) {
+                    const int kb_next = static_cast<int>((u0 + i + C::kQuantWarps) % kg);
+                    for (int line = lane; line < 2 * p.M; line += 32)
+                        prefetch_l1(p.x + static_cast<long long>(line >> 1) * p.ldx + kb_next * 128 + (line & 1) * 64);
+                }
                 // Eight token rows at a time, interleaved so their loads,
                 // reductions and divisions overlap.
                 for (int m0 = 0; m0 < p.M; m0 += 8) {

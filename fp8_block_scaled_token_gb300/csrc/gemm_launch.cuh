@@ -20,15 +20,24 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
         return st;
 
     CUtensorMap tm_w, tm_b;
+    const bool tiled = (L.flags & FP8BS_FLAG_WEIGHTS_TILED) != 0;
+    // Tiled weights are addressed as a [units * 128 rows][128 bytes] matrix.
+    const uint64_t tiled_rows = static_cast<uint64_t>(sh.units) * 128;
     if (MODE == kModeBf16) {
-        st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.N),
-                          static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K) * 2, 64, 128);
+        if (tiled)
+            st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, tiled_rows, 64, 128, 64, 128);
+        else
+            st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.N),
+                              static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K) * 2, 64, 128);
         if (st == FP8BS_OK)
             st = make_tmap_2d(&tm_b, L.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.M),
                               static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.lda) * 2, 64, NPAD);
     } else {
-        st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.N),
-                          static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K), 128, 128);
+        if (tiled)
+            st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, tiled_rows, 128, 128, 128, 128);
+        else
+            st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.N),
+                              static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K), 128, 128);
         if (st == FP8BS_OK) {
             if (MODE == kModeFp8)
                 st = make_tmap_2d(&tm_b, L.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.M),
@@ -59,6 +68,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.counters = reinterpret_cast<unsigned *>(wsb + wl.counters_off);
     p.slots = reinterpret_cast<float *>(wsb + wl.slots_off);
     p.prefetch_before_wait = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
+    p.w_tiled = tiled ? 1 : 0;
     p.test_skip_unit = L.test_skip_unit;
     p.timeout_ns = L.timeout_ns;
 

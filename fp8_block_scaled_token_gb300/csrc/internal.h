@@ -75,8 +75,9 @@ fp8bs_status launch_gemm_bf16(const GemmLaunch &L, const DeviceInfo &dev);
 
 fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, float *xs, bool pdl,
                               cudaStream_t stream);
-fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws,
+fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws, bool tiled,
                                  cudaStream_t stream);
+fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaStream_t stream);
 
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull; // one second
 

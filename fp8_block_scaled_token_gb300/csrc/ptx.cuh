@@ -142,6 +142,12 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x
                  : "memory");
 }
 
+// Fetch the 128-byte line holding `p` into this SM's L1 (no result).
+__device__ __forceinline__ void prefetch_l1(const void *p)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------- global atomics
 // Device-scope add with acquire-release semantics: releases every write
 // that happens-before it (including other threads' writes ordered by a

@@ -39,7 +39,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
         xs[static_cast<long long>(m) * kg + g] = s;
 }
 
-template <bool kBf16>
+// kTiled: write the codes of block (nb, kb) as one contiguous 16 KB run
+// (row r of the block at r*128), rows past N as zeros.
+template <bool kBf16, bool kTiled>
 __global__ void __launch_bounds__(256) quant_weight_kernel(const void *__restrict__ w, int N, int K,
                                                            uint8_t *__restrict__ wq, float *__restrict__ ws)
 {
@@ -86,7 +88,11 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const void *__restric
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int r = r0 + j;
-        if (r < N) {
+        if (kTiled) {
+            const long long off = blk * 16384 + static_cast<long long>(warp * 16 + j) * 128 + lane * 4;
+            *reinterpret_cast<uint32_t *>(wq + off) =
+                r < N ? quantize4(v[j][0], v[j][1], v[j][2], v[j][3], s) : 0u;
+        } else if (r < N) {
             const long long off = static_cast<long long>(r) * K + kb * 128 + lane * 4;
             *reinterpret_cast<uint32_t *>(wq + off) = quantize4(v[j][0], v[j][1], v[j][2], v[j][3], s);
         }
@@ -113,7 +119,38 @@ fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq,
                                             xq, xs));
 }
 
-fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws,
+// bf16 [N][K] -> tiled: tile (nb, kb) of 128 rows x 64 elements is one
+// contiguous 16 KB run, row r at r*128 bytes, rows past N zero.
+__global__ void __launch_bounds__(256) pack_bf16_tiled_kernel(const uint8_t *__restrict__ w, int N, int K,
+                                                              uint8_t *__restrict__ wt)
+{
+    const int kg = K / 64;
+    const long long blk = blockIdx.x;
+    const int nb = static_cast<int>(blk / kg), kb = static_cast<int>(blk % kg);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int idx = j * 256 + threadIdx.x; // 1024 16-byte pieces per tile
+        const int r = idx >> 3, c = idx & 7;
+        const int row = nb * 128 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < N)
+            v = *reinterpret_cast<const uint4 *>(w + static_cast<long long>(row) * K * 2 + kb * 128 + c * 16);
+        *reinterpret_cast<uint4 *>(wt + blk * 16384 + r * 128 + c * 16) = v;
+    }
+}
+
+fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaStream_t stream)
+{
+    const long long blocks = static_cast<long long>((N + 127) / 128) * (K / 64);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    return launch_status(cudaLaunchKernelEx(&cfg, pack_bf16_tiled_kernel, static_cast<const uint8_t *>(w), N, K,
+                                            static_cast<uint8_t *>(wt)));
+}
+
+fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws, bool tiled,
                                  cudaStream_t stream)
 {
     const long long blocks = static_cast<long long>((N + 127) / 128) * (K / 128);
@@ -123,8 +160,10 @@ fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     if (wtype == FP8BS_BF16)
-        return launch_status(cudaLaunchKernelEx(&cfg, quant_weight_kernel<true>, w, N, K, wq, ws));
-    return launch_status(cudaLaunchKernelEx(&cfg, quant_weight_kernel<false>, w, N, K, wq, ws));
+        return launch_status(cudaLaunchKernelEx(&cfg, tiled ? quant_weight_kernel<true, true> : quant_weight_kernel<true, false>,
+                                                w, N, K, wq, ws));
+    return launch_status(cudaLaunchKernelEx(&cfg, tiled ? quant_weight_kernel<false, true> : quant_weight_kernel<false, false>,
+                                            w, N, K, wq, ws));
 }
 
 } // namespace fp8bs

@@ -83,6 +83,13 @@ typedef enum fp8bs_dtype {
  * in flight on `stream` writes the weights or their scales. */
 #define FP8BS_FLAG_OVERLAP_PREV 1u
 
+/* Flag for the GEMM entry points: the weights are in the tiled layout that
+ * fp8_quant_weight_blocks_tiled (FP8) or bf16_pack_weights_tiled (bf16)
+ * writes.  Every 128-row x 128-byte weight tile is then one contiguous 16 KB
+ * run of memory, so each tile the GEMM streams is a single sequential HBM
+ * read instead of 128 separate 128-byte pieces of 128 different rows. */
+#define FP8BS_FLAG_WEIGHTS_TILED 2u
+
 /* Human-readable text of a status code (static storage, never NULL). */
 FP8BS_API const char *fp8bs_status_string(fp8bs_status status);
 
@@ -118,6 +125,17 @@ FP8BS_API fp8bs_status fp8_quant_weight_blocks(const void *w, fp8bs_dtype wtype,
                                      uint8_t *wq, float *ws, void *stream);
 
 /*
+ * The same quantisation (bit-identical codes and scales) written in the tiled
+ * layout: the codes of block (nb, kb) occupy bytes
+ *   [(nb*(K/128) + kb) * 16384, +16384)
+ * with row r of the block (weight row nb*128 + r) at offset r*128, its 128
+ * bytes in K order.  Rows past N in the last block are written as zeros.
+ * wq must hold ceil(N/128) * 128 * K bytes, 16-byte aligned.  ws as above.
+ */
+FP8BS_API fp8bs_status fp8_quant_weight_blocks_tiled(const void *w, fp8bs_dtype wtype, int N, int K,
+                                           uint8_t *wq, float *ws, void *stream);
+
+/*
  * Bytes of device workspace the GEMM entry points need for this shape on the
  * current device (it depends on the SM count).  Writes *bytes; on error
  * writes 0.  The same answer serves fp8_blockscaled_gemm and
@@ -144,7 +162,8 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, 
  * y : bf16 [M][N], 2-byte aligned.
  * 1 <= M <= 64, N >= 1, K >= 128, K % 128 == 0.
  * workspace: device, 256-byte aligned, >= fp8_blockscaled_gemm_workspace_size.
- * flags: 0 or FP8BS_FLAG_OVERLAP_PREV.
+ * flags: any of FP8BS_FLAG_OVERLAP_PREV, FP8BS_FLAG_WEIGHTS_TILED (then wq is
+ * in the tiled layout of fp8_quant_weight_blocks_tiled).
  */
 FP8BS_API fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as,
                                   const uint8_t *wq, const float *ws,
@@ -178,6 +197,14 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx,
  * 1 <= M <= 64, N >= 1, K >= 64, K % 64 == 0.
  */
 FP8BS_API fp8bs_status bf16_gemm_ref_workspace_size(int M, int N, int K, size_t *bytes);
+/*
+ * Copy a bf16 weight matrix [N][K] (K % 64 == 0) into the tiled layout for
+ * bf16_gemm_ref with FP8BS_FLAG_WEIGHTS_TILED: tile (nb, kb) of 128 rows x 64
+ * elements occupies bytes [(nb*(K/64) + kb) * 16384, +16384), row r at
+ * offset r*128; rows past N are zeros.  wt holds ceil(N/128)*128*K*2 bytes.
+ * Both pointers 16-byte aligned.
+ */
+FP8BS_API fp8bs_status bf16_pack_weights_tiled(const void *w, int N, int K, void *wt, void *stream);
 FP8BS_API fp8bs_status bf16_gemm_ref(const void *x, const void *w, void *y,
                            int M, int N, int K,
                            void *workspace, size_t workspace_bytes,

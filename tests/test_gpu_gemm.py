@@ -191,3 +191,32 @@ def test_bf16_gemm_deterministic():
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 5120, 5120), (3, 300, 1280), (64, 640, 2048), (17, 129, 384)])
+def test_tiled_weights_bitwise_equal(M, N, K):
+    x = synth.activations(M, K, seed=M + 7, outlier_p=0.001).cuda()
+    w = synth.weights(N, K, seed=M + 8, outlier_p=0.01).cuda()
+    wq, ws = fb.fp8_quant_weight_blocks(w)
+    wt, _ = fb.fp8_quant_weight_blocks(w, tiled=True)
+    xq, xs = fb.fp8_quant_act(x)
+    for flags in (0, fb.FLAG_OVERLAP_PREV):
+        a = fb.fp8_blockscaled_gemm(xq, xs, wq, ws, flags=flags)
+        b = fb.fp8_blockscaled_gemm(xq, xs, wt, ws, n=N, flags=flags)
+        c = fb.fp8_blockscaled_gemm_fused(x, wt, ws, n=N, flags=flags)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+    ref = oracle_layer(x.cpu(), w.cpu())
+    check_y(b, ref["y"], ref["bound"], "tiled M=%d N=%d K=%d" % (M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 5120, 5120), (5, 300, 640)])
+def test_bf16_tiled_bitwise_equal(M, N, K):
+    x = synth.activations(M, K, seed=90).cuda()
+    w = synth.weights(N, K, seed=91).to(torch.bfloat16).cuda()
+    wt = fb.bf16_pack_weights_tiled(w)
+    a = fb.bf16_gemm_ref(x, w)
+    b = fb.bf16_gemm_ref(x, wt, n=N)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -73,3 +73,35 @@ def test_quant_weight_zero_block_and_ties():
     oq, os_ = oracle.default().quant_weight(w.numpy())
     assert np.array_equal(wq.cpu().numpy(), oq)
     assert np.array_equal(ws.cpu().numpy(), os_)
+
+
+def untile(wt, N, K, block_cols):
+    """Tiled [tiles, 128, block_cols] -> row-major [N, K] (test-side reshaping only)."""
+    kg = K // block_cols
+    nt = wt.shape[0] // kg
+    return wt.view(nt, kg, 128, block_cols).permute(0, 2, 1, 3).reshape(nt * 128, K)[:N]
+
+
+@pytest.mark.parametrize("N,K,dtype", [(256, 512, torch.float32), (300, 1024, torch.float32),
+                                       (200, 384, torch.bfloat16)])
+def test_quant_weight_tiled_layout(N, K, dtype):
+    w = synth.weights(N, K, seed=41, outlier_p=0.01).to(dtype).cuda()
+    wq, ws = fb.fp8_quant_weight_blocks(w)
+    wt, wst = fb.fp8_quant_weight_blocks(w, tiled=True)
+    torch.cuda.synchronize()
+    assert torch.equal(untile(wt, N, K, 128), wq)
+    assert torch.equal(ws, wst)
+    nt = (N + 127) // 128
+    pad = wt.view(nt, K // 128, 128, 128)[-1, :, N - (nt - 1) * 128:, :]
+    assert not pad.any(), "rows past N must be zero in the tiled layout"
+
+
+def test_bf16_pack_tiled_layout():
+    N, K = 300, 640
+    w = synth.weights(N, K, seed=42).to(torch.bfloat16).cuda()
+    wt = fb.bf16_pack_weights_tiled(w)
+    torch.cuda.synchronize()
+    assert torch.equal(untile(wt, N, K, 64).view(torch.int16), w.view(torch.int16))
+    nt = (N + 127) // 128
+    pad = wt.view(nt, K // 64, 128, 64)[-1, :, N - (nt - 1) * 128:, :]
+    assert not pad.view(torch.int16).any()

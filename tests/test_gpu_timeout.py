@@ -1,0 +1,59 @@
+"""Failure detection on the GPU without a fault: every wait in the GEMM
+kernel is bounded.  The test hook makes the producer never fill one pipeline
+stage, so the MMA warp's wait on it runs out; the kernel must record the
+time-out in the workspace status word, free its tensor memory and return, and
+the CUDA context must stay usable for a correct GEMM afterwards."""
+import ctypes
+
+import pytest
+import torch
+
+import fp8_block_scaled_token_gb300 as fb
+from fp8_block_scaled_token_gb300 import synth
+from tests.gpu_helpers import check_y, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT_DEVICE = 7
+
+
+def _stall(xq, xs, wq, ws, y, M, N, K, work, skip_unit, timeout_ns):
+    L = fb.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return L.fp8bs_testhook_gemm_stall(
+        ctypes.c_void_p(xq.data_ptr()), ctypes.c_void_p(xs.data_ptr()), ctypes.c_void_p(wq.data_ptr()),
+        ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(y.data_ptr()), M, N, K,
+        ctypes.c_void_p(work.data_ptr()), work.numel(), skip_unit, timeout_ns, stream)
+
+
+@pytest.mark.parametrize("M,N,K,skip", [(8, 256, 512, 0), (8, 5120, 5120, 3)])
+def test_bounded_wait_reports_timeout_and_context_survives(M, N, K, skip):
+    x = synth.activations(M, K, seed=5)
+    w = synth.weights(N, K, seed=6)
+    xd, wd = x.cuda(), w.cuda()
+    wq, ws = fb.fp8_quant_weight_blocks(wd)
+    xq, xs = fb.fp8_quant_act(xd)
+    y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K))
+    rc = _stall(xq, xs, wq, ws, y, M, N, K, work, skip, 100_000_000)   # 0.1 s limit
+    assert rc == 0, fb.status_string(rc)
+    code = fb.workspace_status(work)                                     # synchronises
+    assert code != 0, "the stalled kernel did not report its time-out"
+    L = fb.lib()
+    c = ctypes.c_int(0)
+    assert L.fp8bs_workspace_status(ctypes.c_void_p(work.data_ptr()), 1, ctypes.byref(c)) == TIMEOUT_DEVICE
+    assert fb.workspace_status(work) == 0                                # cleared
+    # the context is still usable: a normal call on a fresh workspace is correct
+    ref = oracle_layer(x, w)
+    y2 = fb.fp8_blockscaled_gemm(xq, xs, wq, ws)
+    torch.cuda.synchronize()
+    check_y(y2, ref["y"], ref["bound"], "after time-out")
+
+
+def test_stall_hook_rejects_bad_arguments():
+    L = fb.lib()
+    p = ctypes.c_void_p(0x10000)
+    # no skip unit, zero or too-long limit: rejected on the host
+    assert L.fp8bs_testhook_gemm_stall(p, p, p, p, p, 8, 256, 512, p, 1 << 20, -1, 1000, None) == 1
+    assert L.fp8bs_testhook_gemm_stall(p, p, p, p, p, 8, 256, 512, p, 1 << 20, 0, 0, None) == 1
+    assert L.fp8bs_testhook_gemm_stall(p, p, p, p, p, 8, 256, 512, p, 1 << 20, 0, 20_000_000_000, None) == 1
