@@ -104,13 +104,15 @@ fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataTyp
     return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
 }
 
-WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad)
+WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad, int M, int K)
 {
+    auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
     WorkspaceLayout w;
     w.counters_off = 256;
-    const size_t counters = (static_cast<size_t>(ntiles) * 4 + 255) / 256 * 256;
-    w.slots_off = w.counters_off + counters;
-    w.total = w.slots_off + static_cast<size_t>(2) * ctas * npad * 128 * 4;
+    w.slots_off = w.counters_off + up256(static_cast<size_t>(ntiles) * 4);
+    w.act_off = w.slots_off + static_cast<size_t>(2) * ctas * npad * 128 * 4;
+    w.act_scale_off = w.act_off + up256(static_cast<size_t>(M) * K);
+    w.total = w.act_scale_off + up256(static_cast<size_t>(M) * (K / 128) * 4);
     return w;
 }
 
@@ -173,7 +175,7 @@ fp8bs_status gemm_workspace(int mode, int M, int N, int K, size_t *bytes)
     if (st != FP8BS_OK)
         return st;
     const GemmShape sh = gemm_shape(mode, M, N, K, dev.sms);
-    *bytes = workspace_layout(sh.ntiles, sh.ctas, sh.npad).total;
+    *bytes = workspace_layout(sh.ntiles, sh.ctas, sh.npad, M, K).total;
     return FP8BS_OK;
 }
 
@@ -184,7 +186,7 @@ fp8bs_status run_gemm(GemmLaunch &L)
     if (st != FP8BS_OK)
         return st;
     const GemmShape sh = gemm_shape(L.mode, L.M, L.N, L.K, dev.sms);
-    if (L.workspace_bytes < workspace_layout(sh.ntiles, sh.ctas, sh.npad).total)
+    if (L.workspace_bytes < workspace_layout(sh.ntiles, sh.ctas, sh.npad, L.M, L.K).total)
         return FP8BS_ERR_WORKSPACE_TOO_SMALL;
     switch (L.mode) {
     case 0:

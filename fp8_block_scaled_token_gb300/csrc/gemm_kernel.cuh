@@ -7,9 +7,10 @@
 // ran zero times", "The output layer, which did run").
 //
 // Design (one CTA per SM, warp-specialised):
-//   warp 0      TMA producer: streams 128x128-byte weight tiles (and, when
-//               the activations are pre-quantised, the token tile) into an
-//               S-stage shared-memory ring, 128-byte swizzled, no multicast.
+//   warp 0      TMA producer: streams 128-row x 128-byte weight tiles (and,
+//               when the activations are pre-quantised or bf16, the token
+//               tile of the same K block) into an S-stage shared-memory ring,
+//               128-byte swizzled, no multicast.
 //   warp 1      MMA issuer: per 128-wide K block, four tcgen05.mma with the
 //               weights as the 128-row A operand and the tokens (padded to
 //               NPAD = 16/32/48/64) as the B operand, fp32 accumulator in
@@ -19,10 +20,14 @@
 //               s_w[tile,kb] * s_a[m,kb] and adds into fp32 registers; at the
 //               end of a tile it stores bf16 Y, or hands its partial to the
 //               fixed-order K-split reduction.
-//   warps 6+    (fused variant only) activation quantisation: 2 or 4 warps,
-//               each taking every 2nd/4th unit, read the bf16 token rows of that K block,
-//               computes the per-token scale and writes E4M3 codes straight
-//               into the swizzled B-operand tile of the ring stage.
+//   fused only: warps 2-9 first quantise, in the kernel prologue, the token
+//               rows of every K block this CTA will use into an activation
+//               cache in shared memory (E4M3 codes in the swizzled B-operand
+//               layout, plus the per-token scales).  The ring then carries
+//               weights only, and the MMA reads its B operand from the cache.
+//
+// Shared memory: [1 KB barriers and flags][ring: S stages][activation cache]
+// [activation scales]; S and the cache size are chosen per launch.
 //
 // Every wait is bounded; on time-out the CTA records a code in the status
 // word, drains what it has in flight, frees its tensor memory and returns.
@@ -34,10 +39,7 @@
 #include "ptx.cuh"
 #include "quant_math.cuh"
 
-// Shared-memory ring size (KB) and L2 prefetch depth (units); tuning knobs.
-#ifndef FP8BS_RING_KB
-#define FP8BS_RING_KB 200
-#endif
+// L2 prefetch depth (units beyond the ring); a tuning knob, off by default.
 #ifndef FP8BS_PREFETCH_UNITS
 #define FP8BS_PREFETCH_UNITS 0
 #endif
@@ -46,7 +48,7 @@ namespace fp8bs {
 
 enum GemmMode : int {
     kModeFp8 = 0,      // pre-quantised activations (Aq, s_a) read by TMA
-    kModeFp8Fused = 1, // bf16 activations quantised inside the kernel
+    kModeFp8Fused = 1, // bf16 activations quantised in the kernel prologue
     kModeBf16 = 2,     // bf16 x bf16, no block scales
 };
 
@@ -56,6 +58,8 @@ struct GemmParams {
     int ntiles;      // ceil(N / 128)
     long long units; // ntiles * kg
     int ctas;
+    int stages;      // ring depth, <= kMaxStages
+    int act_chunks;  // fused: K blocks in the activation cache (>= distinct K blocks of any CTA)
     const float *as;         // FP8: s_a [M][K/128]
     const float *ws;         // FP8: s_w [ntiles][K/128]
     const uint16_t *x;       // fused: bf16 activations [M][ldx]
@@ -73,44 +77,35 @@ struct GemmParams {
 template <int NPAD, int MODE> struct GemmCfg {
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "token tile");
     static constexpr int kTileRows = 128;                   // weight rows per tile (MMA M)
-    static constexpr int kRowBytes = 128;                   // K bytes per row per stage
+    static constexpr int kRowBytes = 128;                   // K bytes per row per unit
     static constexpr int kChunkElems = MODE == kModeBf16 ? 64 : 128;
     static constexpr int kWBytes = kTileRows * kRowBytes;   // 16 KB
-    static constexpr int kBBytes = NPAD * kRowBytes;        // 2..8 KB
-    static constexpr int kStageBytes = kWBytes + kBBytes;   // multiple of 1024
-    // Ring size: HBM and cross-die L2 latencies on this part are long (over
-    // a microsecond under load), so one CTA per SM with a ~200 KB ring keeps
-    // the most bytes in flight.  A ring of <= 110 KB instead lets a CTA of
-    // the next GEMM (launched early with programmatic dependent launch) share
-    // the SM; the fused kernel at NPAD > 32 needs more registers than that
-    // leaves.  Optional L2 prefetches run further ahead of the ring.
-    static constexpr int kMinBlocks = ((MODE == kModeFp8Fused && NPAD > 32) || FP8BS_RING_KB > 110) ? 1 : 2;
-    static constexpr int kRingBudget = (kMinBlocks == 2 ? FP8BS_RING_KB : (FP8BS_RING_KB > 110 ? FP8BS_RING_KB : 200)) * 1024;
-    static constexpr int kStages = kRingBudget / kStageBytes > 12 ? 12 : kRingBudget / kStageBytes;
-    static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;  // units prefetched into L2 ahead of the ring
+    static constexpr int kBBytes = NPAD * kRowBytes;        // 2..8 KB token tile
+    static constexpr int kStageBytes = kWBytes + (MODE == kModeFp8Fused ? 0 : kBBytes);
+    static constexpr int kMaxStages = 12;
     static constexpr int kAcc = 4;
     static constexpr int kTmemNeed = kAcc * NPAD;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
-    // Quantisation warps of the fused kernel: two suffice up to 32 tokens
-    // (and keep the CTA small enough for two per SM), four above.
-    static constexpr int kQuantWarps = MODE != kModeFp8Fused ? 0 : ((kMinBlocks == 2 && NPAD <= 32) ? 2 : 4);
+    static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
     static constexpr int kEpiWarps = 4;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
-    static constexpr int kSaOffset = kStages * kStageBytes;
-    static constexpr int kSaBytes = MODE == kModeFp8Fused ? kStages * 64 * 4 : 0;
-    static constexpr int kBarOffset = kSaOffset + kSaBytes;
-    static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
-    static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024; // +1024: runtime alignment
+    static constexpr int kHeader = 1024;                    // barriers and flags
+    static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;
     static constexpr int kMmaSteps = kRowBytes / 32;        // 32 bytes of K per tcgen05.mma
+    static constexpr int kActScaleBytes = NPAD * 4;         // per cached K block
     static constexpr uint32_t kIdesc =
         MODE == kModeBf16 ? idesc_bf16_f32(kTileRows, NPAD) : idesc_e4m3_f32(kTileRows, NPAD);
-    static_assert(kStageBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-    static_assert(kStages >= kQuantWarps, "the fused quant warps rely on a ring of at least kQuantWarps stages");
-    static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "shared memory per SM");
+    static_assert(kStageBytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+
+    // Dynamic shared memory of a launch (+1024 for aligning the base).
+    static constexpr int smem_bytes(int stages, int act_chunks)
+    {
+        return 1024 + kHeader + stages * kStageBytes + act_chunks * (kBBytes + kActScaleBytes);
+    }
 };
 
 template <int NPAD, int MODE>
-__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, MODE>::kMinBlocks)
+__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p)
 {
@@ -118,15 +113,19 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
-    uint64_t *empty = full + C::kStages;
-    uint64_t *tfull = empty + C::kStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + C::kMaxStages;
+    uint64_t *tfull = empty + C::kMaxStages;
     uint64_t *tempty = tfull + C::kAcc;
     uint64_t *mma_done = tempty + C::kAcc;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *act_ready = mma_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(act_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
-    float *sa_ring = reinterpret_cast<float *>(smem + C::kSaOffset);
+    const int S = p.stages;
+    uint8_t *ring = smem + C::kHeader;
+    uint8_t *act_cache = ring + S * C::kStageBytes;
+    float *act_scale = reinterpret_cast<float *>(act_cache + p.act_chunks * C::kBBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -134,6 +133,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     const long long u0 = plan_begin(p.units, p.ctas, cta);
     const int nunits = static_cast<int>(plan_begin(p.units, p.ctas, cta + 1) - u0);
     const int kg = p.kg;
+    // The CTA's units cover the cyclic run of K blocks starting at kb0; the
+    // activation-cache slot of its i-th unit is i mod kg.
+    const int kb0 = static_cast<int>(u0 % kg);
     // TMA coordinates of the weight tile of unit u: (K offset, row) in the
     // row-major matrix, or (0, u*128) in the tiled layout where the tiles of
     // consecutive units are consecutive 16 KB runs.
@@ -143,15 +145,16 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], MODE == kModeFp8Fused ? 2 : 1);
-            mbar_init(&empty[s], MODE == kModeFp8Fused ? 1 + C::kEpiWarps : 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < C::kAcc; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], C::kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(act_ready, 1);
         *abort_flag = 0;
         *last_flag = 0;
         fence_mbar_init();
@@ -167,15 +170,10 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
         tmem_relinquish();
     }
     if (MODE == kModeFp8Fused) {
-        // Token rows >= M of every B tile, and their scales, stay zero for the
-        // whole kernel.
-        for (int i = threadIdx.x; i < C::kStages * (C::kBBytes / 16); i += C::kThreads) {
-            const int s = i / (C::kBBytes / 16), o = i % (C::kBBytes / 16);
-            reinterpret_cast<uint4 *>(smem + s * C::kStageBytes + C::kWBytes)[o] = make_uint4(0, 0, 0, 0);
-        }
-        for (int i = threadIdx.x; i < C::kStages * 64; i += C::kThreads)
-            sa_ring[i] = 0.0f;
-        fence_proxy_async_smem();
+        // Token rows >= M of every cached B tile, and their scales, stay zero.
+        const int n16 = p.act_chunks * ((C::kBBytes + C::kActScaleBytes) / 16);
+        for (int i = threadIdx.x; i < n16; i += C::kThreads)
+            reinterpret_cast<uint4 *>(act_cache)[i] = make_uint4(0, 0, 0, 0);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -190,16 +188,16 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_b = l2_policy_evict_last();
-            const uint32_t tx = C::kWBytes + (MODE == kModeFp8Fused ? 0 : C::kBBytes);
+            const uint32_t tx = C::kStageBytes;
             uint32_t armed_mask = 0, armed_parity = 0;
-            const int pre = p.prefetch_before_wait ? (nunits < C::kStages ? nunits : C::kStages) : 0;
+            const int pre = p.prefetch_before_wait ? (nunits < S ? nunits : S) : 0;
             // Units beyond the first ring pass go to L2 ahead of time (once the
             // weights may be read: before the dependency wait only with the
             // overlap flag).
-            int prefetched = C::kStages;
+            int prefetched = S;
             bool weights_readable = p.prefetch_before_wait != 0;
             auto prefetch_upto = [&](int limit) {
-                if (!weights_readable)
+                if (C::kPrefetch == 0 || !weights_readable)
                     return;
                 for (; prefetched < limit && prefetched < nunits; ++prefetched) {
                     const long long u = u0 + prefetched;
@@ -213,44 +211,56 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const long long u = u0 + i;
                 mbar_arrive_expect_tx(&full[i], tx);
                 armed_mask |= 1u << i;
-                tma_load_2d(smem + i * C::kStageBytes, &tm_w, &full[i], w_x(u), w_y(u), pol_w);
+                tma_load_2d(ring + i * C::kStageBytes, &tm_w, &full[i], w_x(u), w_y(u), pol_w);
             }
             prefetch_upto(pre + C::kPrefetch);
             grid_dependency_wait();
-            weights_readable = true;  // the previous grid has completed
+            weights_readable = true; // the previous grid has completed
             if (MODE != kModeFp8Fused) {
                 for (int i = 0; i < pre; ++i) {
                     if (i == p.test_skip_unit)
                         continue;
                     const int kb = static_cast<int>((u0 + i) % kg);
-                    tma_load_2d(smem + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb * C::kChunkElems, 0,
+                    tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb * C::kChunkElems, 0,
                                 pol_b);
                 }
             }
+            // Per-unit state advances by increments: no divisions in this
+            // single-thread loop, whose latency sets the issue rate.
+            int s = pre % S;
+            uint32_t ph = static_cast<uint32_t>(pre / S) & 1u;
+            int kb = static_cast<int>((u0 + pre) % kg);
+            int tile = static_cast<int>((u0 + pre) / kg);
             for (int i = pre; i < nunits; ++i) {
-                const int s = i % C::kStages;
-                const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutProducer, p.timeout_ns))
                     break;
-                if (i == p.test_skip_unit)
-                    continue;
-                const long long u = u0 + i;
-                const int kb = static_cast<int>(u % kg);
-                mbar_arrive_expect_tx(&full[s], tx);
-                armed_mask |= 1u << s;
-                armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
-                tma_load_2d(smem + s * C::kStageBytes, &tm_w, &full[s], w_x(u), w_y(u), pol_w);
-                if (MODE != kModeFp8Fused)
-                    tma_load_2d(smem + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems, 0,
-                                pol_b);
-                // keep the L2 prefetch kPrefetch units ahead of the ring, once
-                // the first ring pass has been requested
-                if (i + 1 >= C::kStages)
-                    prefetch_upto(i + 1 + C::kPrefetch);
+                if (i != p.test_skip_unit) {
+                    mbar_arrive_expect_tx(&full[s], tx);
+                    armed_mask |= 1u << s;
+                    armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                    const int wx = p.w_tiled ? 0 : kb * C::kChunkElems;
+                    const int wy = p.w_tiled ? (tile * kg + kb) * C::kTileRows : tile * C::kTileRows;
+                    tma_load_2d(ring + s * C::kStageBytes, &tm_w, &full[s], wx, wy, pol_w);
+                    if (MODE != kModeFp8Fused)
+                        tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems, 0,
+                                    pol_b);
+                    // keep the L2 prefetch kPrefetch units ahead of the ring, once
+                    // the first ring pass has been requested
+                    if (C::kPrefetch > 0 && i + 1 >= S)
+                        prefetch_upto(i + 1 + C::kPrefetch);
+                }
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (++kb == kg) {
+                    kb = 0;
+                    ++tile;
+                }
             }
             // Nothing may still be landing in shared memory when the CTA exits:
             // wait (bounded) for the last phase armed on every stage.
-            for (int s = 0; s < C::kStages; ++s) {
+            for (int s = 0; s < S; ++s) {
                 if (!(armed_mask & (1u << s)))
                     continue;
                 const uint32_t ph = (armed_parity >> s) & 1u;
@@ -268,10 +278,22 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
         if (lane == 0) {
             int acc = 0;
             uint32_t acc_ph = 0;
-            for (int i = 0; i < nunits; ++i) {
-                const int s = i % C::kStages;
-                const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
-                const int kb = static_cast<int>((u0 + i) % kg);
+            bool ok = true;
+            if (MODE == kModeFp8Fused)
+                ok = mbar_wait(act_ready, 0, abort_flag, p.status, kErrTimeoutMma, p.timeout_ns);
+            int s = 0, kb = kb0, slot = 0;
+            uint32_t ph = 0;
+            for (int i = 0; ok && i < nunits; ++i) {
+                if (i > 0) {
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++kb == kg)
+                        kb = 0;
+                    if (++slot == kg)
+                        slot = 0;
+                }
                 const bool seg_start = (i == 0) || (kb == 0);
                 const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
                 // FP8: every K block gets a fresh accumulator (its scale differs);
@@ -285,8 +307,10 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NPAD);
-                const uint64_t a_desc = sw128_kmajor_desc(smem_u32(smem + s * C::kStageBytes));
-                const uint64_t b_desc = sw128_kmajor_desc(smem_u32(smem + s * C::kStageBytes + C::kWBytes));
+                const uint64_t a_desc = sw128_kmajor_desc(smem_u32(ring + s * C::kStageBytes));
+                const uint8_t *b_tile = MODE == kModeFp8Fused ? act_cache + slot * C::kBBytes
+                                                              : ring + s * C::kStageBytes + C::kWBytes;
+                const uint64_t b_desc = sw128_kmajor_desc(smem_u32(b_tile));
 #pragma unroll
                 for (int k = 0; k < C::kMmaSteps; ++k) {
                     const uint32_t accumulate = (k > 0 || !fresh) ? 1u : 0u;
@@ -315,148 +339,155 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 }
             }
         }
-    } else if (warp < 2 + C::kEpiWarps) {
-        // ------------------------------------------------ promotion / epilogue
-        const int quarter = warp & 3;             // TMEM lanes this warp may read
-        const int row = quarter * 32 + lane;      // weight row within the tile
-        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        float acc[NPAD];
-#pragma unroll
-        for (int m = 0; m < NPAD; ++m)
-            acc[m] = 0.0f;
-        int accb = 0;
-        uint32_t acc_ph = 0;
-        int seg_first_kb = 0;
+    } else {
         grid_dependency_wait();
-        for (int i = 0; i < nunits; ++i) {
-            const long long u = u0 + i;
-            const int tile = static_cast<int>(u / kg), kb = static_cast<int>(u % kg);
-            const bool seg_start = (i == 0) || (kb == 0);
-            const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
-            const int s = i % C::kStages;
-            if (seg_start)
-                seg_first_kb = kb;
-            if (MODE != kModeBf16 || seg_end) {
-                float sw = 1.0f, sa0 = 0.0f, sa1 = 0.0f;
-                if (MODE != kModeBf16)
-                    sw = p.ws[static_cast<long long>(tile) * kg + kb];
-                if (MODE == kModeFp8) {
-                    if (lane < p.M)
-                        sa0 = p.as[static_cast<long long>(lane) * kg + kb];
-                    if (lane + 32 < p.M)
-                        sa1 = p.as[static_cast<long long>(lane + 32) * kg + kb];
-                }
-                mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
-                if (MODE == kModeFp8Fused) {
-                    // Acquire the quantisation warp's writes of this stage's
-                    // scales (that phase is complete once the MMA has run).
-                    mbar_wait(&full[s], static_cast<uint32_t>(i / C::kStages) & 1u, abort_flag, p.status,
-                              kErrTimeoutEpilogue, p.timeout_ns);
-                }
-                named_bar_sync(1, 32 * C::kEpiWarps);
-                if (*abort_flag)
-                    break; // uniform across the four epilogue warps
-                tc_fence_after_sync();
-                const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD);
-#pragma unroll
-                for (int c = 0; c < NPAD / 16; ++c) {
-                    uint32_t r[16];
-                    tmem_load16(taddr + c * 16, r);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int m = c * 16 + j;
-                        const float d = __uint_as_float(r[j]);
-                        if (MODE == kModeBf16) {
-                            acc[m] = d;
-                        } else {
-                            float sam;
-                            if (MODE == kModeFp8Fused)
-                                sam = sa_ring[s * 64 + m];
-                            else
-                                sam = __shfl_sync(0xffffffffu, m < 32 ? sa0 : sa1, m & 31);
-                            acc[m] = fmaf(sw * sam, d, acc[m]);
-                        }
+        if constexpr (MODE == kModeFp8Fused) {
+            // -------------------------------------------- prologue: activation cast
+            // Warps 2-9 quantise every (cached K block, token) row once: item
+            // j = chunk * M + m, eight consecutive items per warp at a time so
+            // their loads, reductions and divisions overlap.
+            const int qw = warp - 2;
+            constexpr int kQW = C::kEpiWarps + C::kQuantWarps;
+            const int total = p.act_chunks * p.M;
+            // Pull every row this warp will read into L1 first (one L2 round
+            // trip for all of them).
+            for (int j0 = qw * 8; j0 < total; j0 += kQW * 8)
+                if (lane < 16) {
+                    const int j = j0 + (lane >> 1);
+                    if (j < total) {
+                        const int c = j / p.M, m = j - c * p.M;
+                        const int kb = kb0 + c < kg ? kb0 + c : kb0 + c - kg;
+                        prefetch_l1(p.x + static_cast<long long>(m) * p.ldx + kb * 128 + (lane & 1) * 64);
                     }
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&tempty[accb]);
-                    if (MODE == kModeFp8Fused)
-                        mbar_arrive(&empty[s]);
+            for (int j0 = qw * 8; j0 < total; j0 += kQW * 8) {
+                uint2 raw[8];
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const int j = j0 + b;
+                    raw[b] = make_uint2(0u, 0u);
+                    if (j < total) {
+                        const int c = j / p.M, m = j - c * p.M;
+                        const int kb = kb0 + c < kg ? kb0 + c : kb0 + c - kg;
+                        raw[b] = *reinterpret_cast<const uint2 *>(p.x + static_cast<long long>(m) * p.ldx +
+                                                                  kb * 128 + lane * 4);
+                    }
                 }
-                if (++accb == C::kAcc) {
-                    accb = 0;
-                    acc_ph ^= 1u;
+                float v[8][4], am[8];
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    v[b][0] = bf16_lo(raw[b].x);
+                    v[b][1] = bf16_hi(raw[b].x);
+                    v[b][2] = bf16_lo(raw[b].y);
+                    v[b][3] = bf16_hi(raw[b].y);
+                    am[b] = abs_max4(v[b][0], v[b][1], v[b][2], v[b][3]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int b = 0; b < 8; ++b)
+                        am[b] = fmaxf(am[b], __shfl_xor_sync(0xffffffffu, am[b], o));
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const int j = j0 + b;
+                    if (j >= total)
+                        break; // warp-uniform
+                    const int c = j / p.M, m = j - c * p.M;
+                    const float sc = group_scale(am[b]);
+                    const uint32_t codes = quantize4(v[b][0], v[b][1], v[b][2], v[b][3], sc);
+                    // row m, bytes 4*lane..4*lane+3 of its 128-byte row; the
+                    // 16-byte chunk index is XOR-ed with (row mod 8) as TMA's
+                    // 128-byte swizzle does.
+                    const uint32_t off =
+                        static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) + ((lane & 3) << 2));
+                    *reinterpret_cast<uint32_t *>(act_cache + c * C::kBBytes + off) = codes;
+                    if (lane == 0)
+                        act_scale[c * NPAD + m] = sc;
                 }
             }
-            if (!seg_end)
-                continue;
-            // ---- tile segment complete: store or reduce
-            const int n = tile * C::kTileRows + row;
-            const bool whole_tile = (seg_first_kb == 0) && (kb == kg - 1);
-            if (whole_tile) {
-                if (n < p.N) {
+            fence_proxy_async_smem(); // codes are read by the tensor core
+            named_bar_sync(2, 32 * kQW);
+            if (warp == 2 && lane == 0)
+                mbar_arrive(act_ready);
+        }
+        if (warp < 2 + C::kEpiWarps) {
+            // -------------------------------------------- promotion / epilogue
+            const int quarter = warp & 3;             // TMEM lanes this warp may read
+            const int row = quarter * 32 + lane;      // weight row within the tile
+            const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+            float acc[NPAD];
 #pragma unroll
-                    for (int m = 0; m < NPAD; ++m)
-                        if (m < p.M)
-                            p.y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+            for (int m = 0; m < NPAD; ++m)
+                acc[m] = 0.0f;
+            int accb = 0;
+            uint32_t acc_ph = 0;
+            int seg_first_kb = 0;
+            int tile = static_cast<int>(u0 / kg), kb = kb0, slot = 0;
+            for (int i = 0; i < nunits; ++i) {
+                if (i > 0) {
+                    if (++kb == kg) {
+                        kb = 0;
+                        ++tile;
+                    }
+                    if (++slot == kg)
+                        slot = 0;
                 }
-            } else {
-                // K-split tile: publish this CTA's partial, and the last
-                // contributor to arrive sums all of them in contributor order.
-                const long long t_first = static_cast<long long>(tile) * kg;
-                const int c_first = plan_owner(p.units, p.ctas, t_first);
-                const int c_last = plan_owner(p.units, p.ctas, t_first + kg - 1);
-                float *mine = p.slots + static_cast<long long>(plan_slot(p.units, p.ctas, kg, cta, tile)) * (NPAD * 128);
+                const bool seg_start = (i == 0) || (kb == 0);
+                const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
+                if (seg_start)
+                    seg_first_kb = kb;
+                if (MODE != kModeBf16 || seg_end) {
+                    float sw = 1.0f, sa0 = 0.0f, sa1 = 0.0f;
+                    if (MODE != kModeBf16)
+                        sw = p.ws[static_cast<long long>(tile) * kg + kb];
+                    if (MODE == kModeFp8) {
+                        if (lane < p.M)
+                            sa0 = p.as[static_cast<long long>(lane) * kg + kb];
+                        if (lane + 32 < p.M)
+                            sa1 = p.as[static_cast<long long>(lane + 32) * kg + kb];
+                    }
+                    const float *sa_c = act_scale + (MODE == kModeFp8Fused ? slot * NPAD : 0);
+                    mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
+                    named_bar_sync(1, 32 * C::kEpiWarps);
+                    if (*abort_flag)
+                        break; // uniform across the four epilogue warps
+                    tc_fence_after_sync();
+                    const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD);
 #pragma unroll
-                for (int m = 0; m < NPAD; ++m)
-                    if (m < p.M)
-                        __stcg(mine + m * 128 + row, acc[m]);
-                named_bar_sync(1, 32 * C::kEpiWarps);
-                if (warp == 2 && lane == 0) {
-                    // one release for the whole epilogue group's stores (ordered
-                    // by the barrier above); acquire for the others' partials
-                    const unsigned prev = atomic_add_acq_rel_gpu(&p.counters[tile], 1u);
-                    *last_flag = (prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
-                }
-                named_bar_sync(1, 32 * C::kEpiWarps);
-                if (*last_flag) {
+                    for (int c = 0; c < NPAD / 16; ++c) {
+                        uint32_t r[16];
+                        tmem_load16(taddr + c * 16, r);
 #pragma unroll
-                    for (int m = 0; m < NPAD; ++m)
-                        acc[m] = 0.0f;
-                    // Issue every contributor's loads for a chunk of tokens at
-                    // once (one L2 round trip per chunk), then add them in
-                    // contributor order.
-                    constexpr int kMaxC = 6;
-                    constexpr int kMC = NPAD <= 16 ? 16 : 8;
-                    for (int c0 = c_first; c0 <= c_last; c0 += kMaxC) {
-                        const int nc = c_last - c0 + 1 < kMaxC ? c_last - c0 + 1 : kMaxC;
-                        const float *src[kMaxC];
-#pragma unroll
-                        for (int j = 0; j < kMaxC; ++j)
-                            src[j] = p.slots +
-                                     static_cast<long long>(plan_slot(p.units, p.ctas, kg, c0 + (j < nc ? j : 0), tile)) *
-                                         (NPAD * 128) +
-                                     row;
-#pragma unroll
-                        for (int mc = 0; mc < NPAD; mc += kMC) {
-                            if (mc >= p.M)
-                                break;
-                            float v[kMaxC][kMC];
-#pragma unroll
-                            for (int j = 0; j < kMaxC; ++j)
-#pragma unroll
-                                for (int q = 0; q < kMC; ++q)
-                                    v[j][q] = (j < nc && mc + q < p.M) ? __ldcg(src[j] + (mc + q) * 128) : 0.0f;
-#pragma unroll
-                            for (int j = 0; j < kMaxC; ++j)
-#pragma unroll
-                                for (int q = 0; q < kMC; ++q)
-                                    if (j < nc)
-                                        acc[mc + q] += v[j][q];
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = c * 16 + j;
+                            const float d = __uint_as_float(r[j]);
+                            if (MODE == kModeBf16) {
+                                acc[m] = d;
+                            } else {
+                                float sam;
+                                if (MODE == kModeFp8Fused)
+                                    sam = sa_c[m];
+                                else
+                                    sam = __shfl_sync(0xffffffffu, m < 32 ? sa0 : sa1, m & 31);
+                                acc[m] = fmaf(sw * sam, d, acc[m]);
+                            }
                         }
                     }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&tempty[accb]);
+                    if (++accb == C::kAcc) {
+                        accb = 0;
+                        acc_ph ^= 1u;
+                    }
+                }
+                if (!seg_end)
+                    continue;
+                // ---- tile segment complete: store or reduce
+                const int n = tile * C::kTileRows + row;
+                const bool whole_tile = (seg_first_kb == 0) && (kb == kg - 1);
+                if (whole_tile) {
                     if (n < p.N) {
 #pragma unroll
                         for (int m = 0; m < NPAD; ++m)
@@ -464,79 +495,78 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                                 p.y[static_cast<long long>(m) * p.N + n] =
                                     __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
                     }
-                    if (warp == 2 && lane == 0)
-                        p.counters[tile] = 0u; // ready for the next call
-                }
-                named_bar_sync(1, 32 * C::kEpiWarps);
-            }
+                } else {
+                    // K-split tile: publish this CTA's partial, and the last
+                    // contributor to arrive sums all of them in contributor order.
+                    const long long t_first = static_cast<long long>(tile) * kg;
+                    const int c_first = plan_owner(p.units, p.ctas, t_first);
+                    const int c_last = plan_owner(p.units, p.ctas, t_first + kg - 1);
+                    float *mine =
+                        p.slots + static_cast<long long>(plan_slot(p.units, p.ctas, kg, cta, tile)) * (NPAD * 128);
 #pragma unroll
-            for (int m = 0; m < NPAD; ++m)
-                acc[m] = 0.0f;
-        }
-    } else {
-        // ------------------------------------------------ fused activation quantisation
-        if constexpr (MODE == kModeFp8Fused) {
-            const int qw = warp - 2 - C::kEpiWarps;
-            grid_dependency_wait();
-            for (int i = qw; i < nunits; i += C::kQuantWarps) {
-                const int s = i % C::kStages;
-                const uint32_t ph = static_cast<uint32_t>(i / C::kStages) & 1u;
-                if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutQuant, p.timeout_ns))
-                    break;
-                const int kb = static_cast<int>((u0 + i) % kg);
-                const uint16_t *xk = p.x + static_cast<long long>(kb) * 128 + lane * 4;
-                uint8_t *btile = smem + s * C::kStageBytes + C::kWBytes;
-                // Pull the token rows of this warp's next unit into L1 now, so
-                // their loads do not wait a full L2 round trip later.
-                if (i + C::kQuantWarps < nunits) {
-                    const int kb_next = static_cast<int>((u0 + i + C::kQuantWarps) % kg);
-                    for (int line = lane; line < 2 * p.M; line += 32)
-                        prefetch_l1(p.x + static_cast<long long>(line >> 1) * p.ldx + kb_next * 128 + (line & 1) * 64);
-                }
-                // Eight token rows at a time, interleaved so their loads,
-                // reductions and divisions overlap.
-                for (int m0 = 0; m0 < p.M; m0 += 8) {
-                    uint2 raw[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        raw[j] = (m0 + j < p.M)
-                                     ? *reinterpret_cast<const uint2 *>(xk + static_cast<long long>(m0 + j) * p.ldx)
-                                     : make_uint2(0u, 0u);
-                    float v[8][4], am[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        v[j][0] = bf16_lo(raw[j].x);
-                        v[j][1] = bf16_hi(raw[j].x);
-                        v[j][2] = bf16_lo(raw[j].y);
-                        v[j][3] = bf16_hi(raw[j].y);
-                        am[j] = abs_max4(v[j][0], v[j][1], v[j][2], v[j][3]);
+                    for (int m = 0; m < NPAD; ++m)
+                        if (m < p.M)
+                            __stcg(mine + m * 128 + row, acc[m]);
+                    named_bar_sync(1, 32 * C::kEpiWarps);
+                    if (warp == 2 && lane == 0) {
+                        // one release for the whole epilogue group's stores (ordered
+                        // by the barrier above); acquire for the others' partials
+                        const unsigned prev = atomic_add_acq_rel_gpu(&p.counters[tile], 1u);
+                        *last_flag = (prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
                     }
+                    named_bar_sync(1, 32 * C::kEpiWarps);
+                    if (*last_flag) {
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
+                        for (int m = 0; m < NPAD; ++m)
+                            acc[m] = 0.0f;
+                        // Issue every contributor's loads for a chunk of tokens at
+                        // once (one L2 round trip per chunk), then add them in
+                        // contributor order.
+                        constexpr int kMaxC = 6;
+                        constexpr int kMC = NPAD <= 16 ? 16 : 8;
+                        for (int c0 = c_first; c0 <= c_last; c0 += kMaxC) {
+                            const int nc = c_last - c0 + 1 < kMaxC ? c_last - c0 + 1 : kMaxC;
+                            const float *src[kMaxC];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
+                            for (int j = 0; j < kMaxC; ++j)
+                                src[j] = p.slots +
+                                         static_cast<long long>(
+                                             plan_slot(p.units, p.ctas, kg, c0 + (j < nc ? j : 0), tile)) *
+                                             (NPAD * 128) +
+                                         row;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int m = m0 + j;
-                        if (m >= p.M)
-                            break; // warp-uniform; rows >= M stay zero
-                        const float sc = group_scale(am[j]);
-                        const uint32_t codes = quantize4(v[j][0], v[j][1], v[j][2], v[j][3], sc);
-                        // row m, bytes 4*lane..4*lane+3 of its 128-byte row; the
-                        // 16-byte chunk index is XOR-ed with (row mod 8) as TMA's
-                        // 128-byte swizzle does.
-                        const uint32_t off =
-                            static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) + ((lane & 3) << 2));
-                        *reinterpret_cast<uint32_t *>(btile + off) = codes;
-                        if (lane == 0)
-                            sa_ring[s * 64 + m] = sc;
+                            for (int mc = 0; mc < NPAD; mc += kMC) {
+                                if (mc >= p.M)
+                                    break;
+                                float v[kMaxC][kMC];
+#pragma unroll
+                                for (int j = 0; j < kMaxC; ++j)
+#pragma unroll
+                                    for (int q = 0; q < kMC; ++q)
+                                        v[j][q] = (j < nc && mc + q < p.M) ? __ldcg(src[j] + (mc + q) * 128) : 0.0f;
+#pragma unroll
+                                for (int j = 0; j < kMaxC; ++j)
+#pragma unroll
+                                    for (int q = 0; q < kMC; ++q)
+                                        if (j < nc)
+                                            acc[mc + q] += v[j][q];
+                            }
+                        }
+                        if (n < p.N) {
+#pragma unroll
+                            for (int m = 0; m < NPAD; ++m)
+                                if (m < p.M)
+                                    p.y[static_cast<long long>(m) * p.N + n] =
+                                        __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                        }
+                        if (warp == 2 && lane == 0)
+                            p.counters[tile] = 0u; // ready for the next call
                     }
+                    named_bar_sync(1, 32 * C::kEpiWarps);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&full[s]);
+#pragma unroll
+                for (int m = 0; m < NPAD; ++m)
+                    acc[m] = 0.0f;
             }
         }
     }

@@ -8,14 +8,44 @@
 
 namespace fp8bs {
 
+constexpr int kSmemLimit = 227 * 1024;      // dynamic shared memory per CTA
+constexpr int kRingBudget = 200 * 1024;     // ring of the non-fused kernels
+constexpr int kActCacheBudget = 96 * 1024;  // fused: activation cache + scales
+
+// Ring depth and activation-cache size of a launch; act_chunks < 0 means the
+// fused kernel's cache would not fit (the caller then quantises separately).
+template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stages, int &act_chunks)
+{
+    using C = GemmCfg<NPAD, MODE>;
+    act_chunks = 0;
+    int ring = kRingBudget;
+    if (MODE == kModeFp8Fused) {
+        const long long per_cta = (sh.units + sh.ctas - 1) / sh.ctas;
+        act_chunks = static_cast<int>(per_cta < sh.kg ? per_cta : sh.kg);
+        if (act_chunks * (C::kBBytes + C::kActScaleBytes) > kActCacheBudget) {
+            act_chunks = -1;
+            stages = 0;
+            return;
+        }
+        ring = kSmemLimit - C::smem_bytes(0, act_chunks);
+    }
+    stages = ring / C::kStageBytes;
+    if (stages > C::kMaxStages)
+        stages = C::kMaxStages;
+}
+
 template <int NPAD, int MODE>
 fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
 {
     using C = GemmCfg<NPAD, MODE>;
     static unsigned long long attr_done = 0;
     auto kernel = gemm_small_m_kernel<NPAD, MODE>;
-    fp8bs_status st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), C::kSmemBytes, dev.device,
-                                       &attr_done);
+    int stages = 0, act_chunks = 0;
+    gemm_smem_plan<NPAD, MODE>(sh, stages, act_chunks);
+    if (act_chunks < 0 || stages < 2)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE; // not reached: the fused launcher checks first
+    const int smem = C::smem_bytes(stages, act_chunks);
+    fp8bs_status st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), kSmemLimit, dev.device, &attr_done);
     if (st != FP8BS_OK)
         return st;
 
@@ -49,7 +79,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     if (st != FP8BS_OK)
         return st;
 
-    const WorkspaceLayout wl = workspace_layout(sh.ntiles, sh.ctas, NPAD);
+    const WorkspaceLayout wl = workspace_layout(sh.ntiles, sh.ctas, NPAD, L.M, L.K);
     uint8_t *wsb = static_cast<uint8_t *>(L.workspace);
     GemmParams p;
     p.M = L.M;
@@ -59,6 +89,8 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.ntiles = sh.ntiles;
     p.units = sh.units;
     p.ctas = sh.ctas;
+    p.stages = stages;
+    p.act_chunks = act_chunks;
     p.as = L.as;
     p.ws = L.ws;
     p.x = static_cast<const uint16_t *>(MODE == kModeFp8Fused ? L.a : nullptr);
@@ -75,7 +107,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), 1, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -83,6 +115,27 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     cfg.attrs = attr;
     cfg.numAttrs = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
     return launch_status(cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_b, p));
+}
+
+// True when the fused kernel's activation cache fits for this shape.
+template <int MODE> bool fused_cache_fits(const GemmShape &sh)
+{
+    int stages = 0, act_chunks = 0;
+    switch (sh.npad) {
+    case 16:
+        gemm_smem_plan<16, MODE>(sh, stages, act_chunks);
+        break;
+    case 32:
+        gemm_smem_plan<32, MODE>(sh, stages, act_chunks);
+        break;
+    case 48:
+        gemm_smem_plan<48, MODE>(sh, stages, act_chunks);
+        break;
+    default:
+        gemm_smem_plan<64, MODE>(sh, stages, act_chunks);
+        break;
+    }
+    return act_chunks >= 0 && stages >= 2;
 }
 
 template <int MODE>

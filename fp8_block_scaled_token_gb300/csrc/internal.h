@@ -39,11 +39,13 @@ inline int token_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 
 // Workspace layout shared by the GEMM launchers:
 //   [0, 256)                status word (+ padding)
 //   [256, 256 + C)          ntiles 32-bit arrival counters, C rounded up to 256
-//   [256 + C, ...)          2 * ctas slots of NPAD * 128 fp32 partials
+//   slots                   2 * ctas slots of NPAD * 128 fp32 partials
+//   act, act_scale          M x K codes and M x K/128 scales, used only when the
+//                           fused entry point quantises in a separate kernel
 struct WorkspaceLayout {
-    size_t counters_off, slots_off, total;
+    size_t counters_off, slots_off, act_off, act_scale_off, total;
 };
-WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad);
+WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad, int M, int K);
 
 struct GemmLaunch {
     int mode;                 // GemmMode

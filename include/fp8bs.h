@@ -173,11 +173,14 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as,
 
 /*
  * The whole layer from bf16 activations: activation quantisation (as
- * fp8_quant_act) fused with the GEMM (as fp8_blockscaled_gemm).  The
- * quantised activations are formed inside the GEMM kernel, per 128-wide K
- * block, straight into shared memory in the tensor-core operand layout; they
- * never reach global memory.  Bitwise identical to fp8_quant_act followed by
- * fp8_blockscaled_gemm on the same inputs.
+ * fp8_quant_act) fused with the GEMM (as fp8_blockscaled_gemm).  In the GEMM
+ * kernel's prologue every CTA quantises the token rows of the K blocks it
+ * will use straight into a shared-memory cache in the tensor-core operand
+ * layout, so the quantised activations never reach global memory.  When that
+ * cache would exceed 96 KB (ceil(units per SM) x NPAD x 128 bytes, i.e. large
+ * M and K), the call instead runs the quantisation as its own kernel into the
+ * workspace, followed by the pre-quantised GEMM.  Either way the result is
+ * bitwise identical to fp8_quant_act followed by fp8_blockscaled_gemm.
  * x: bf16, M rows, row stride ldx elements, 16-byte aligned, ldx % 8 == 0.
  * Other arguments as fp8_blockscaled_gemm.
  */
