@@ -191,6 +191,29 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx,
                                         unsigned flags, void *stream);
 
 /*
+ * fp8_blockscaled_gemm_fused without a caller-provided workspace, for callers
+ * that cannot allocate device memory (code running under a graph capture
+ * that must not allocate, allocator-less embedded runtimes, hooks that run
+ * while a framework holds its memory pool).  The pages have no counterpart:
+ * this is an interface convenience, not part of the method.
+ * The split-K scratch lives in a 12 MiB array inside the library (every GPU
+ * that loads the library holds it until the process exits); shapes whose
+ * workspace (fp8_blockscaled_gemm_workspace_size) exceeds 12 MiB are rejected
+ * with FP8BS_ERR_UNSUPPORTED_SHAPE.  The call allocates nothing.  Its first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress),
+ * so make that first call before any stream capture.  Each call clears the
+ * array's status word and counters on `stream` before the kernel runs; every
+ * call shares the one array, so calls that can overlap on the GPU (different
+ * streams without ordering) race and must not be issued.  Device-side
+ * time-outs are recorded in the shared array and are not reported back.
+ * Arguments and result as fp8_blockscaled_gemm_fused.
+ */
+FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ldx,
+                                                const uint8_t *wq, const float *ws,
+                                                void *y, int M, int N, int K,
+                                                unsigned flags, void *stream);
+
+/*
  * 16-bit comparison GEMM for the output layer [P2 "The output layer, which
  * did run": the layer "still 16-bit" before conversion]:
  *   y[m*N + n] = bf16_rn( sum_k x[m,k] * w[n,k] )   (fp32 accumulation)
