@@ -124,6 +124,7 @@ GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
     s.units = static_cast<long long>(s.ntiles) * s.kg;
     s.ctas = plan_ctas(s.units, sms);
     s.npad = token_pad(M);
+    s.m = M;
     return s;
 }
 

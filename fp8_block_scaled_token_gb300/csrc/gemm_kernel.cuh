@@ -34,6 +34,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <type_traits>
 
 #include "plan.cuh"
 #include "ptx.cuh"
@@ -197,11 +198,13 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
             int prefetched = S;
             bool weights_readable = p.prefetch_before_wait != 0;
             auto prefetch_upto = [&](int limit) {
-                if (C::kPrefetch == 0 || !weights_readable)
-                    return;
-                for (; prefetched < limit && prefetched < nunits; ++prefetched) {
-                    const long long u = u0 + prefetched;
-                    tma_prefetch_l2_2d(&tm_w, w_x(u), w_y(u));
+                if constexpr (C::kPrefetch > 0) {
+                    if (!weights_readable)
+                        return;
+                    for (; prefetched < limit && prefetched < nunits; ++prefetched) {
+                        const long long u = u0 + prefetched;
+                        tma_prefetch_l2_2d(&tm_w, w_x(u), w_y(u));
+                    }
                 }
             };
             // Weights for the first ring pass, possibly before the previous grid is done.
@@ -349,28 +352,34 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
             const int qw = warp - 2;
             constexpr int kQW = C::kEpiWarps + C::kQuantWarps;
             const int total = p.act_chunks * p.M;
-            // Pull every row this warp will read into L1 first (one L2 round
-            // trip for all of them).
-            for (int j0 = qw * 8; j0 < total; j0 += kQW * 8)
-                if (lane < 16) {
-                    const int j = j0 + (lane >> 1);
-                    if (j < total) {
-                        const int c = j / p.M, m = j - c * p.M;
-                        const int kb = kb0 + c < kg ? kb0 + c : kb0 + c - kg;
-                        prefetch_l1(p.x + static_cast<long long>(m) * p.ldx + kb * 128 + (lane & 1) * 64);
-                    }
-                }
-            for (int j0 = qw * 8; j0 < total; j0 += kQW * 8) {
+            // Items go round-robin over the warps (item j to warp j % kQW), and
+            // each warp takes its items eight at a time.  First ask for every
+            // row this warp will read to be brought into L1.
+            for (int j = qw + kQW * lane; j < total; j += kQW * 32) {
+                const int c = j / p.M, m = j - c * p.M;
+                const int kbj = kb0 + c < kg ? kb0 + c : kb0 + c - kg;
+                const uint16_t *row_ptr = p.x + static_cast<long long>(m) * p.ldx + kbj * 128;
+                prefetch_l1(row_ptr);
+                prefetch_l1(row_ptr + 64);
+            }
+            // One batch: this warp's items j0, j0 + kQW, ... (n of them; n == 8
+            // except in the last batch).  Full batches take a straight-line
+            // path so the eight items' loads, reductions and conversions
+            // overlap; only the tail guards each item.
+            auto cast_batch = [&](int j0, int n, auto full_batch) {
+                constexpr bool kFull = decltype(full_batch)::value;
                 uint2 raw[8];
+                int cs[8], ms[8];
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    const int j = j0 + b;
+                    const int j = j0 + b * kQW;
+                    cs[b] = j / p.M;
+                    ms[b] = j - cs[b] * p.M;
                     raw[b] = make_uint2(0u, 0u);
-                    if (j < total) {
-                        const int c = j / p.M, m = j - c * p.M;
-                        const int kb = kb0 + c < kg ? kb0 + c : kb0 + c - kg;
-                        raw[b] = *reinterpret_cast<const uint2 *>(p.x + static_cast<long long>(m) * p.ldx +
-                                                                  kb * 128 + lane * 4);
+                    if (kFull || b < n) {
+                        const int kbj = kb0 + cs[b] < kg ? kb0 + cs[b] : kb0 + cs[b] - kg;
+                        raw[b] = *reinterpret_cast<const uint2 *>(p.x + static_cast<long long>(ms[b]) * p.ldx +
+                                                                  kbj * 128 + lane * 4);
                     }
                 }
                 float v[8][4], am[8];
@@ -380,30 +389,32 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                     v[b][1] = bf16_hi(raw[b].x);
                     v[b][2] = bf16_lo(raw[b].y);
                     v[b][3] = bf16_hi(raw[b].y);
-                    am[b] = abs_max4(v[b][0], v[b][1], v[b][2], v[b][3]);
+                    am[b] = warp_max(abs_max4(v[b][0], v[b][1], v[b][2], v[b][3]));
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                    for (int b = 0; b < 8; ++b)
-                        am[b] = fmaxf(am[b], __shfl_xor_sync(0xffffffffu, am[b], o));
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    const int j = j0 + b;
-                    if (j >= total)
-                        break; // warp-uniform
-                    const int c = j / p.M, m = j - c * p.M;
-                    const float sc = group_scale(am[b]);
-                    const uint32_t codes = quantize4(v[b][0], v[b][1], v[b][2], v[b][3], sc);
-                    // row m, bytes 4*lane..4*lane+3 of its 128-byte row; the
-                    // 16-byte chunk index is XOR-ed with (row mod 8) as TMA's
-                    // 128-byte swizzle does.
-                    const uint32_t off =
-                        static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) + ((lane & 3) << 2));
-                    *reinterpret_cast<uint32_t *>(act_cache + c * C::kBBytes + off) = codes;
-                    if (lane == 0)
-                        act_scale[c * NPAD + m] = sc;
+                    if (kFull || b < n) {
+                        const int m = ms[b];
+                        const float sc = group_scale(am[b]);
+                        const uint32_t codes = quantize4(v[b][0], v[b][1], v[b][2], v[b][3], sc);
+                        // row m, bytes 4*lane..4*lane+3 of its 128-byte row; the
+                        // 16-byte chunk index is XOR-ed with (row mod 8) as TMA's
+                        // 128-byte swizzle does.
+                        const uint32_t off = static_cast<uint32_t>(m * 128 + ((((lane >> 2) ^ (m & 7)) & 7) << 4) +
+                                                                   ((lane & 3) << 2));
+                        *reinterpret_cast<uint32_t *>(act_cache + cs[b] * C::kBBytes + off) = codes;
+                        if (lane == 0)
+                            act_scale[cs[b] * NPAD + m] = sc;
+                    }
                 }
+            };
+            const int mine = total > qw ? (total - qw + kQW - 1) / kQW : 0; // items of this warp
+            for (int t = 0; t < mine; t += 8) {
+                const int j0 = qw + t * kQW;
+                if (t + 8 <= mine)
+                    cast_batch(j0, 8, std::true_type{});
+                else
+                    cast_batch(j0, mine - t, std::false_type{});
             }
             fence_proxy_async_smem(); // codes are read by the tensor core
             named_bar_sync(2, 32 * kQW);
@@ -423,6 +434,27 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
             uint32_t acc_ph = 0;
             int seg_first_kb = 0;
             int tile = static_cast<int>(u0 / kg), kb = kb0, slot = 0;
+            // Reduction plans of the (at most two) tiles this CTA may share:
+            // the tile its range starts in and the one it ends in.  Worked out
+            // once here, off the critical path, so the end-of-tile exchange
+            // does no 64-bit division.  Contributors are the consecutive CTAs
+            // c_first..c_last; each uses slot 2c, except that c_first uses
+            // 2c+1 when its range began in an earlier tile.
+            struct SplitPlan {
+                int c_first, c_last, slot_first;
+            };
+            auto make_plan = [&](int t) {
+                const long long tf = static_cast<long long>(t) * kg;
+                SplitPlan sp;
+                sp.c_first = plan_owner(p.units, p.ctas, tf);
+                sp.c_last = plan_owner(p.units, p.ctas, tf + kg - 1);
+                sp.slot_first = 2 * sp.c_first + (plan_begin(p.units, p.ctas, sp.c_first) == tf ? 0 : 1);
+                return sp;
+            };
+            const int tile_a = tile;
+            const int tile_b = static_cast<int>((u0 + nunits - 1) / kg);
+            const SplitPlan plan_a = make_plan(tile_a);
+            const SplitPlan plan_b = tile_b != tile_a ? make_plan(tile_b) : plan_a;
             for (int i = 0; i < nunits; ++i) {
                 if (i > 0) {
                     if (++kb == kg) {
@@ -498,11 +530,10 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                 } else {
                     // K-split tile: publish this CTA's partial, and the last
                     // contributor to arrive sums all of them in contributor order.
-                    const long long t_first = static_cast<long long>(tile) * kg;
-                    const int c_first = plan_owner(p.units, p.ctas, t_first);
-                    const int c_last = plan_owner(p.units, p.ctas, t_first + kg - 1);
-                    float *mine =
-                        p.slots + static_cast<long long>(plan_slot(p.units, p.ctas, kg, cta, tile)) * (NPAD * 128);
+                    const SplitPlan &pl = tile == tile_a ? plan_a : plan_b;
+                    const int c_first = pl.c_first, c_last = pl.c_last;
+                    auto slot_of = [&](int c) { return c == c_first ? pl.slot_first : 2 * c; };
+                    float *mine = p.slots + static_cast<long long>(slot_of(cta)) * (NPAD * 128);
 #pragma unroll
                     for (int m = 0; m < NPAD; ++m)
                         if (m < p.M)
@@ -529,10 +560,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
                             const float *src[kMaxC];
 #pragma unroll
                             for (int j = 0; j < kMaxC; ++j)
-                                src[j] = p.slots +
-                                         static_cast<long long>(
-                                             plan_slot(p.units, p.ctas, kg, c0 + (j < nc ? j : 0), tile)) *
-                                             (NPAD * 128) +
+                                src[j] = p.slots + static_cast<long long>(slot_of(c0 + (j < nc ? j : 0))) * (NPAD * 128) +
                                          row;
 #pragma unroll
                             for (int mc = 0; mc < NPAD; mc += kMC) {

@@ -11,6 +11,10 @@ namespace fp8bs {
 constexpr int kSmemLimit = 227 * 1024;      // dynamic shared memory per CTA
 constexpr int kRingBudget = 200 * 1024;     // ring of the non-fused kernels
 constexpr int kActCacheBudget = 96 * 1024;  // fused: activation cache + scales
+// fused: above this many (K block, token) rows per CTA the prologue cast costs
+// more than a separate cast kernel (every CTA quantises its own K blocks, so
+// the work is replicated across CTAs); measured on GB300.
+constexpr int kPrologueMaxRows = 128;
 
 // Ring depth and activation-cache size of a launch; act_chunks < 0 means the
 // fused kernel's cache would not fit (the caller then quantises separately).
@@ -22,7 +26,8 @@ template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stag
     if (MODE == kModeFp8Fused) {
         const long long per_cta = (sh.units + sh.ctas - 1) / sh.ctas;
         act_chunks = static_cast<int>(per_cta < sh.kg ? per_cta : sh.kg);
-        if (act_chunks * (C::kBBytes + C::kActScaleBytes) > kActCacheBudget) {
+        if (act_chunks * (C::kBBytes + C::kActScaleBytes) > kActCacheBudget ||
+            act_chunks * sh.m > kPrologueMaxRows) {
             act_chunks = -1;
             stages = 0;
             return;

@@ -66,7 +66,7 @@ struct GemmLaunch {
 
 // Shape and SM count -> schedule; shared by launch and size queries.
 struct GemmShape {
-    int kg, ntiles, ctas, npad;
+    int kg, ntiles, ctas, npad, m;
     long long units;
 };
 GemmShape gemm_shape(int mode, int M, int N, int K, int sms);

@@ -35,12 +35,10 @@ FP8BS_HD int plan_owner(long long units, int ctas, long long u)
 }
 
 // A CTA contributes a partial to at most two tiles: the one its range starts
-// in and the one it ends in.  Slot 2c holds the first, 2c+1 the second.
-FP8BS_HD int plan_slot(long long units, int ctas, int kg, int c, long long tile)
-{
-    const long long first_tile = plan_begin(units, ctas, c) / kg;
-    return 2 * c + (tile == first_tile ? 0 : 1);
-}
+// in and the one it ends in.  Slot 2c holds the first, 2c+1 the second (a CTA
+// whose range lies inside one tile uses 2c).  So the contributors c_first <
+// c <= c_last of a tile use slot 2c, and c_first uses 2c_first + 1 unless its
+// range begins exactly at the tile's first unit.
 
 FP8BS_HD int plan_ctas(long long units, int sms)
 {

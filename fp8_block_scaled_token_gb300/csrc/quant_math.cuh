@@ -42,16 +42,38 @@ __device__ __forceinline__ float abs_max4(float a, float b, float c, float d)
     return fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(d)));
 }
 
+// Maximum over the warp of a non-negative float (an absolute value).  For
+// non-negative IEEE values the unsigned bit patterns order like the values,
+// so one unsigned warp reduction gives the exact maximum.
 __device__ __forceinline__ float warp_max(float v)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
+// Codes of four values of one group: e4m3 of the correctly rounded fp32
+// quotient x / scale.
+//
+// Fast path: q = x * rcp(scale) is within a few fp32 ulps of x / scale, and
+// the interval [q - |q|e, q + |q|e] with e = 2^-19 contains both the exact
+// quotient and its fp32 rounding.  E4M3 rounding is monotonic, so when both
+// ends of the interval convert to the same code, every value inside it does,
+// and that code is exactly the one of the correctly rounded quotient.  Only
+// when an E4M3 rounding boundary falls inside the interval (about one value
+// in 2^15) is the IEEE division done.  A subnormal scale (all |x| below
+// 448 * 2^-126) always takes the exact path.
 __device__ __forceinline__ uint32_t quantize4(float a, float b, float c, float d, float scale)
 {
+    if (scale < 1.17549435e-38f) // subnormal scale: reciprocal not accurate enough
+        return e4m3x4(__fdiv_rn(a, scale), __fdiv_rn(b, scale), __fdiv_rn(c, scale), __fdiv_rn(d, scale));
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(scale));
+    const float qa = a * r, qb = b * r, qc = c * r, qd = d * r;
+    constexpr float kE = 1.0f / 524288.0f; // 2^-19
+    const float ea = fabsf(qa) * kE, eb = fabsf(qb) * kE, ec = fabsf(qc) * kE, ed = fabsf(qd) * kE;
+    const uint32_t lo = e4m3x4(qa - ea, qb - eb, qc - ec, qd - ed);
+    const uint32_t hi = e4m3x4(qa + ea, qb + eb, qc + ec, qd + ed);
+    if (lo == hi)
+        return lo;
     return e4m3x4(__fdiv_rn(a, scale), __fdiv_rn(b, scale), __fdiv_rn(c, scale), __fdiv_rn(d, scale));
 }
 

@@ -176,11 +176,13 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as,
  * fp8_quant_act) fused with the GEMM (as fp8_blockscaled_gemm).  In the GEMM
  * kernel's prologue every CTA quantises the token rows of the K blocks it
  * will use straight into a shared-memory cache in the tensor-core operand
- * layout, so the quantised activations never reach global memory.  When that
- * cache would exceed 96 KB (ceil(units per SM) x NPAD x 128 bytes, i.e. large
- * M and K), the call instead runs the quantisation as its own kernel into the
- * workspace, followed by the pre-quantised GEMM.  Either way the result is
- * bitwise identical to fp8_quant_act followed by fp8_blockscaled_gemm.
+ * layout, so the quantised activations never reach global memory.  Every CTA
+ * quantises its own K blocks, so this work is replicated across the SMs; when
+ * a CTA would have more than 128 (K block, token) rows to cast, or its cache
+ * would exceed 96 KB, the call instead runs the quantisation once as its own
+ * kernel into the workspace, followed by the pre-quantised GEMM.  Either way
+ * the result is bitwise identical to fp8_quant_act followed by
+ * fp8_blockscaled_gemm.
  * x: bf16, M rows, row stride ldx elements, 16-byte aligned, ldx % 8 == 0.
  * Other arguments as fp8_blockscaled_gemm.
  */
