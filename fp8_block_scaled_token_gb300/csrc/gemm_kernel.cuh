@@ -88,6 +88,13 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kTmemNeed = kAcc * NPAD;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
     static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
+    // Up to 16 tokens the non-fused kernels run two CTAs per SM (a ~100 KB
+    // ring each): the next GEMM's CTA, launched early by programmatic
+    // dependent launch, then shares the SM and streams its weights while this
+    // one finishes.  Measured on GB300 this beats one CTA per SM with a
+    // 200 KB ring for every layer shape of the workloads at M <= 16, and
+    // loses at M = 32 (and the wider accumulators of NPAD >= 48 would spill).
+    static constexpr int kMinBlocks = (MODE != kModeFp8Fused && NPAD == 16) ? 2 : 1;
     static constexpr int kEpiWarps = 4;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kHeader = 1024;                    // barriers and flags
@@ -106,7 +113,7 @@ template <int NPAD, int MODE> struct GemmCfg {
 };
 
 template <int NPAD, int MODE>
-__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, MODE>::kMinBlocks)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p)
 {

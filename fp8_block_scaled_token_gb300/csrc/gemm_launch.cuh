@@ -9,12 +9,16 @@
 namespace fp8bs {
 
 constexpr int kSmemLimit = 227 * 1024;      // dynamic shared memory per CTA
-constexpr int kRingBudget = 200 * 1024;     // ring of the non-fused kernels
+constexpr int kRingBudget = 200 * 1024;     // ring of a kernel that has the SM to itself
+constexpr int kSharedRingBudget = 100 * 1024; // ring of a kernel that runs two CTAs per SM
 constexpr int kActCacheBudget = 96 * 1024;  // fused: activation cache + scales
 // fused: above this many (K block, token) rows per CTA the prologue cast costs
-// more than a separate cast kernel (every CTA quantises its own K blocks, so
-// the work is replicated across CTAs); measured on GB300.
-constexpr int kPrologueMaxRows = 128;
+// more than a separate cast kernel: the prologue can only start once the
+// previous kernel has produced the activations, and every CTA repeats it for
+// its own K blocks, while the separate kernel casts each row once and the
+// GEMM streams weights meanwhile.  Measured on GB300 (5,120^2 at M = 8:
+// 13.9 us with the prologue, 11.9 us with the separate kernel; equal at M = 1).
+constexpr int kPrologueMaxRows = 16;
 
 // Ring depth and activation-cache size of a launch; act_chunks < 0 means the
 // fused kernel's cache would not fit (the caller then quantises separately).
@@ -22,7 +26,7 @@ template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stag
 {
     using C = GemmCfg<NPAD, MODE>;
     act_chunks = 0;
-    int ring = kRingBudget;
+    int ring = C::kMinBlocks == 2 ? kSharedRingBudget : kRingBudget;
     if (MODE == kModeFp8Fused) {
         const long long per_cta = (sh.units + sh.ctas - 1) / sh.ctas;
         act_chunks = static_cast<int>(per_cta < sh.kg ? per_cta : sh.kg);

@@ -178,9 +178,10 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as,
  * will use straight into a shared-memory cache in the tensor-core operand
  * layout, so the quantised activations never reach global memory.  Every CTA
  * quantises its own K blocks, so this work is replicated across the SMs; when
- * a CTA would have more than 128 (K block, token) rows to cast, or its cache
+ * a CTA would have more than 16 (K block, token) rows to cast, or its cache
  * would exceed 96 KB, the call instead runs the quantisation once as its own
- * kernel into the workspace, followed by the pre-quantised GEMM.  Either way
+ * kernel into the workspace, followed by the pre-quantised GEMM (faster on
+ * GB300 beyond that size).  Either way
  * the result is bitwise identical to fp8_quant_act followed by
  * fp8_blockscaled_gemm.
  * x: bf16, M rows, row stride ldx elements, 16-byte aligned, ldx % 8 == 0.

@@ -72,10 +72,10 @@ def test_closed_form_constant():
 
 
 def test_fused_is_bitwise_the_two_kernel_path():
-    # the first three use the in-kernel prologue cast, the last two the
-    # separate cast kernel (too many rows per CTA for the prologue)
-    for M, N, K, seed in ((8, 5120, 5120, 1), (33, 1000, 3072, 21), (64, 256, 512, 22), (64, 5120, 5120, 25),
-                          (16, 2048, 17408, 26)):
+    # the first three cast in the kernel prologue (at most 16 rows per CTA),
+    # the others through the separate cast kernel
+    for M, N, K, seed in ((1, 5120, 5120, 27), (2, 2048, 1024, 28), (16, 640, 2048, 29), (8, 5120, 5120, 1),
+                          (33, 1000, 3072, 21), (64, 256, 512, 22), (64, 5120, 5120, 25), (16, 2048, 17408, 26)):
         x = synth.activations(M, K, seed=seed, outlier_p=0.001).cuda()
         w = synth.weights(N, K, seed=seed + 1).cuda()
         a = gpu_layer(x, w, fused=False)
