@@ -22,6 +22,10 @@ What each function follows is stated in ``oracle.c``.  In brief:
   128-wide K block, with the error-bound reference sum |a||w|.
 * ``gemm_bf16`` -- the 16-bit output-layer product of the same page, fp64.
 * ``round_bf16`` -- one fp64 -> bf16 rounding, nearest-even.
+* ``greedy`` -- the greedy next-token choice the output layer feeds ("The
+  profiler said the kernel ran zero times", section "The output layer, which
+  did run"): per token, the column of the largest bf16 logit, lowest column on
+  ties.
 
 Every function here has at least one pin in ``tests/test_oracle_*.py``.
 """
@@ -81,6 +85,8 @@ class Oracle:
         L.oracle_gemm_bf16.restype = _int
         L.oracle_gemm_bf16.argtypes = [_u16p, _u16p, _int, _int, _int,
                                        _i32p, _int, _f64p, _f64p, _int]
+        L.oracle_greedy.restype = _int
+        L.oracle_greedy.argtypes = [_u16p, _int, _int, _int, _i32p, _f32p]
         self.lib = L
         self.path = path
 
@@ -220,6 +226,24 @@ class Oracle:
         return {"xq": xq, "xs": xs, "wq": wq, "ws": ws, "y": y, "bound": bound}
 
 
+    # -- greedy token choice ----------------------------------------------------
+    def greedy(self, y_bf16_bits, N=None):
+        """Per token row of bf16 logits (uint16 bit patterns [M, ldy]): the
+        column of the largest value among the first N (all when None), lowest
+        column on ties, +0 == -0.  Returns (token int32 [M], logit float32 [M],
+        a zero logit reported as +0)."""
+        y = np.ascontiguousarray(np.asarray(y_bf16_bits, dtype=np.uint16))
+        M, ldy = y.shape
+        N = ldy if N is None else int(N)
+        token = np.empty(M, dtype=np.int32)
+        logit = np.empty(M, dtype=np.float32)
+        rc = self.lib.oracle_greedy(_ptr(y, ctypes.c_uint16), M, N, ldy, _ptr(token, ctypes.c_int),
+                                    _ptr(logit, ctypes.c_float))
+        if rc != 0:
+            raise ValueError("oracle_greedy: bad shape or NaN logits")
+        return token, logit
+
+
 _default = None
 
 
@@ -239,6 +263,6 @@ def mutant(n: int) -> Oracle:
 def __getattr__(name):
     # Module-level shortcuts: oracle.quant_act(...) == oracle.default().quant_act(...)
     if name in ("e4m3_decode_table", "e4m3_encode", "round_bf16", "f32_to_bf16_bits",
-                "quant_act", "quant_weight", "gemm_fp8", "gemm_bf16", "linear_fp8"):
+                "quant_act", "quant_weight", "gemm_fp8", "gemm_bf16", "linear_fp8", "greedy"):
         return getattr(default(), name)
     raise AttributeError(name)

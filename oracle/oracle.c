@@ -446,3 +446,43 @@ uint16_t oracle_f32_to_bf16(float v)
 {
     return oracle_round_bf16((double)v);
 }
+
+/* ------------------------------------------------------------------ */
+/* Greedy token choice over the output layer's logits.                  */
+/* ------------------------------------------------------------------ */
+/* The output layer feeds the greedy choice of the next token ("The profiler
+   said the kernel ran zero times", section "The output layer, which did
+   run").  Reading taken: for each token row m of the bf16 logits
+   Y [M rows, row stride ldy] (bit patterns), token[m] = the column n < N of
+   the largest value, compared as numbers (+0 equals -0); among equal values
+   the lowest n.  logit[m] (optional) = that largest value, with a zero
+   reported as +0.  NaN logits are outside the contract: -1. */
+int oracle_greedy(const uint16_t *y, int M, int N, int ldy, int32_t *token, float *logit)
+{
+    if (M < 0 || N < 1 || ldy < N)
+        return -1;
+    for (int m = 0; m < M; ++m) {
+        const uint16_t *row = y + (size_t)m * ldy;
+        int best = 0;
+        float bv = bf16_to_f32(row[0]);
+        for (int n = 0; n < N; ++n) {
+            float v = bf16_to_f32(row[n]);
+            if (isnan(v))
+                return -1;
+#if ORACLE_MUTANT == 12
+            if (v >= bv) {                 /* mutant: ties go to the highest column */
+#elif ORACLE_MUTANT == 13
+            if (v > bv || (v == bv && signbit(bv) && !signbit(v))) { /* mutant: -0 below +0 */
+#else
+            if (v > bv) {
+#endif
+                best = n;
+                bv = v;
+            }
+        }
+        token[m] = best;
+        if (logit)
+            logit[m] = bv == 0.0f ? 0.0f : bv;
+    }
+    return 0;
+}

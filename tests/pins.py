@@ -407,4 +407,47 @@ def pin_gemm_bf16_bruteforce(o):
     assert np.allclose(bound, np.abs(X) @ np.abs(W).T, rtol=1e-12)
 
 
+# ---------------------------------------------------------------- greedy choice
+def _bf16_bits_of(values):
+    t = torch.tensor(np.asarray(values, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_greedy_vs_numpy_argmax(o):
+    # numpy's argmax returns the first of equal maxima and compares -0 == +0:
+    # the same rule, computed by a library routine.  Small integers make ties
+    # (and signed zeros) frequent.
+    rng = np.random.default_rng(51)
+    vals = rng.integers(-6, 7, size=(9, 700)).astype(np.float32)
+    vals[rng.random(vals.shape) < 0.2] *= -0.0   # zeros of both signs, negatives flipped
+    vals[3] = -vals[3] - 1.0                     # an all-negative row
+    bits = _bf16_bits_of(vals)
+    tok, logit = o.greedy(bits)
+    ref = np.argmax(vals.astype(np.float64), axis=1)
+    assert np.array_equal(tok, ref)
+    assert np.array_equal(logit, vals.max(axis=1) + np.float32(0.0))
+
+
+def pin_greedy_hand_cases(o):
+    rows = [
+        ([1.0, 3.0, 3.0, 2.0], 1, 3.0),
+        ([-0.0, 0.0, -1.0], 0, 0.0),            # -0 equals +0: the lower column
+        ([-5.0, -1.0, -1.0], 1, -1.0),
+        ([2.0, 2.0, 2.0, 2.0], 0, 2.0),
+        ([0.5, 0.25, 448.0, 1e30], 3, 1e30),
+    ]
+    for vals, want, wlogit in rows:
+        tok, logit = o.greedy(_bf16_bits_of([vals]))
+        assert tok[0] == want, vals
+        assert float(logit[0]) == float(torch.tensor(wlogit).to(torch.bfloat16).float())
+        assert not np.signbit(logit[0]) or logit[0] != 0
+
+
+def pin_greedy_first_n_columns(o):
+    # columns at or past N are not candidates
+    bits = _bf16_bits_of([[1.0, 2.0, 9.0, 9.0], [4.0, 4.0, 9.0, 0.0]])
+    tok, _ = o.greedy(bits, N=2)
+    assert list(tok) == [1, 0]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

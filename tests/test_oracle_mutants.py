@@ -20,6 +20,8 @@ MUTANTS = {
     9: "gemm: weight operand read transposed",
     10: "encode: sign of zero dropped",
     11: "encode: overflow to NaN instead of saturating",
+    12: "greedy: ties to the highest column",
+    13: "greedy: -0 ranked below +0",
 }
 
 
