@@ -460,6 +460,50 @@ def time_graph(fn, reps_inner, reps_outer, stream):
     return s.elapsed_time(e) * 1e3 / (reps_inner * reps_outer)
 
 
+PASS_SHAPES = ((5120, 5120), (34816, 5120), (5120, 17408), (7168, 5120))  # (N, K)
+
+
+def decode_pass(dev, stream, peak, Ms=(1, 2, 4, 8, 16, 32, 64)):
+    """One decode pass: 256 GEMMs cycling the four layer shapes, every one with
+    its own weights (22.4 GB, seeds 100 + i), then the output layer; timed as
+    one graph per token count M."""
+    import torch
+
+    import fp8_block_scaled_token_gb300 as fb
+    from fp8_block_scaled_token_gb300 import synth
+    layers = []
+    for i in range(256):
+        N, K = PASS_SHAPES[i % 4]
+        w = synth.weights(N, K, seed=100 + i, device=dev)
+        layers.append((N, K) + fb.fp8_quant_weight_blocks(w, tiled=True))
+        del w
+    vN, vK = workload("vocab")["N"], workload("vocab")["K"]
+    w = synth.weights(vN, vK, seed=356, device=dev)
+    layers.append((vN, vK) + fb.fp8_quant_weight_blocks(w, tiled=True))
+    del w
+    torch.cuda.synchronize()
+    rows = []
+    for M in Ms:
+        xs = {K: synth.activations(M, K, seed=1, device=dev) for K in (5120, 17408)}
+        ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for N, _ in PASS_SHAPES + ((vN, vK),)}
+        wsz = max(fb.fp8_blockscaled_gemm_workspace_size(M, N, K) for N, K, _, _ in layers)
+        work = fb.make_workspace(wsz, dev)
+
+        def f(i, xs=xs, ys=ys, work=work):
+            for N, K, wq, ws in layers:
+                fb.fp8_blockscaled_gemm_fused(xs[K], wq, ws, y=ys[N], workspace=work, flags=fb.FLAG_OVERLAP_PREV,
+                                              n=N)
+        us = time_graph(f, 1, 20, stream)
+        b = sum(algorithmic_bytes(M, N, K) for N, K, _, _ in layers)
+        rows.append({"workload": "decode_pass_257", "M": M, "ms": round(us / 1e3, 4),
+                     "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
+        print(json.dumps(rows[-1]), file=sys.stderr, flush=True)
+        del xs, ys, work
+    del layers
+    torch.cuda.empty_cache()
+    return rows
+
+
 def sweep(args, dev):
     import torch
 
@@ -491,8 +535,23 @@ def sweep(args, dev):
             out.append({"workload": name, "M": M, "N": N, "K": K, "us": round(us, 3),
                         "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
             print(json.dumps(out[-1]), file=sys.stderr, flush=True)
+            if name == "vocab":
+                # the output layer with the greedy token choice fused, logits not stored
+                tok = torch.empty((M,), dtype=torch.int32, device=dev)
+                lg = torch.empty((M,), dtype=torch.float32, device=dev)
+
+                def g(i, x=x, work=work, N=N, tok=tok, lg=lg):
+                    wq, ws = layers[i % R]
+                    fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, store_y=False, token=tok, logit=lg,
+                                                         workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
+                us = time_graph(g, R, max(1, 400 // R), stream)
+                b = algorithmic_bytes(M, N, K) - 2 * M * N  # no Y written
+                out.append({"workload": "vocab_greedy", "M": M, "N": N, "K": K, "us": round(us, 3),
+                            "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
+                print(json.dumps(out[-1]), file=sys.stderr, flush=True)
         del layers
         torch.cuda.empty_cache()
+    out += decode_pass(dev, stream, peak)
     # vocab layer in bf16 (the 16-bit baseline of the output layer)
     cfg = workload("vocab")
     N, K = cfg["N"], cfg["K"]

@@ -53,6 +53,7 @@ def lib():
         "fp8_blockscaled_gemm_workspace_size": [i, i, i, ctypes.POINTER(sz)],
         "fp8_blockscaled_gemm": [vp, vp, vp, vp, vp, i, i, i, vp, sz, u, vp],
         "fp8_blockscaled_gemm_fused": [vp, i, vp, vp, vp, i, i, i, vp, sz, u, vp],
+        "fp8_blockscaled_gemm_fused_greedy": [vp, i, vp, vp, vp, i, i, i, vp, vp, vp, sz, u, vp],
         "bf16_gemm_ref_workspace_size": [i, i, i, ctypes.POINTER(sz)],
         "bf16_gemm_ref": [vp, vp, vp, i, i, i, vp, sz, u, vp],
         "fp8bs_workspace_status": [vp, i, ctypes.POINTER(i)],
@@ -242,6 +243,43 @@ def fp8_blockscaled_gemm_fused(x, wq, ws, y=None, workspace=None, flags=0, n=Non
            lib().fp8_blockscaled_gemm_fused(_ptr(x), x.stride(0), _ptr(wq), _ptr(ws), _ptr(y), M, N, K,
                                             _ptr(workspace), workspace.numel(), flags, _stream()))
     return y
+
+
+def fp8_blockscaled_gemm_fused_greedy(x, wq, ws, y=None, store_y=True, token=None, logit=None, workspace=None,
+                                      flags=0, n=None):
+    """The fused layer plus the greedy next-token choice per token row:
+    returns (token int32 [M], logit fp32 [M], y bf16 [M,N] or None).  With
+    ``store_y=False`` the logits are not written (y must then be None)."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    _rows_contiguous(x, "x")
+    _need(wq, torch.uint8, "wq", ndim=wq.dim() if wq.dim() in (2, 3) else 2)
+    _need(ws, torch.float32, "ws")
+    M, K = x.shape
+    N, tf = _weight_dims(wq, K, n, "wq")
+    flags |= tf
+    if tuple(ws.shape) != ((N + 127) // 128, K // 128):
+        raise ValueError("operand shapes do not agree")
+    if not store_y and y is not None:
+        raise ValueError("store_y=False takes no y")
+    if store_y and y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if token is None:
+        token = torch.empty((M,), dtype=torch.int32, device=x.device)
+    if logit is None:
+        logit = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _need(token, torch.int32, "token", ndim=1)
+    _need(logit, torch.float32, "logit", ndim=1)
+    if token.numel() < M or logit.numel() < M:
+        raise ValueError("token and logit need M entries")
+    if workspace is None:
+        workspace = make_workspace(fp8_blockscaled_gemm_workspace_size(M, N, K), x.device)
+    _check("fp8_blockscaled_gemm_fused_greedy",
+           lib().fp8_blockscaled_gemm_fused_greedy(_ptr(x), x.stride(0), _ptr(wq), _ptr(ws),
+                                                   _ptr(y) if y is not None else None, M, N, K, _ptr(token),
+                                                   _ptr(logit), _ptr(workspace), workspace.numel(), flags,
+                                                   _stream()))
+    return token, logit, y
 
 
 def bf16_gemm_ref(x, w, y=None, workspace=None, flags=0, n=None):

@@ -108,7 +108,8 @@ WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad, int M, int K)
 {
     auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
     WorkspaceLayout w;
-    w.counters_off = 256;
+    w.greedy_off = 256;
+    w.counters_off = 1024;
     w.slots_off = w.counters_off + up256(static_cast<size_t>(ntiles) * 4);
     w.act_off = w.slots_off + static_cast<size_t>(2) * ctas * npad * 128 * 4;
     w.act_scale_off = w.act_off + up256(static_cast<size_t>(M) * K);
@@ -353,6 +354,42 @@ fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx, const uint8_t *w
     L.w = wq;
     L.ws = ws;
     L.y = y;
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    L.flags = flags;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.test_skip_unit = -1;
+    L.timeout_ns = kDefaultTimeoutNs;
+    return run_gemm(L);
+}
+
+fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx, const uint8_t *wq, const float *ws,
+                                               void *y, int M, int N, int K, int32_t *token, float *logit,
+                                               void *workspace, size_t workspace_bytes, unsigned flags,
+                                               void *stream)
+{
+    if (!x || !wq || !ws || !token || !workspace)
+        return FP8BS_ERR_INVALID_ARG;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
+        return FP8BS_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||
+        !aligned(token, 4) || !aligned(logit, 4) || !aligned(workspace, 256))
+        return FP8BS_ERR_MISALIGNED;
+    GemmLaunch L = {};
+    L.mode = 1;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.a = x;
+    L.lda = ldx;
+    L.w = wq;
+    L.ws = ws;
+    L.y = y;
+    L.token = token;
+    L.logit = logit;
     L.workspace = workspace;
     L.workspace_bytes = workspace_bytes;
     L.flags = flags;

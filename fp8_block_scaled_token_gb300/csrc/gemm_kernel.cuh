@@ -20,6 +20,12 @@
 //               s_w[tile,kb] * s_a[m,kb] and adds into fp32 registers; at the
 //               end of a tile it stores bf16 Y, or hands its partial to the
 //               fixed-order K-split reduction.
+//   greedy (optional, the output layer): while storing a finished tile the
+//               epilogue warps also pick, per token, the tile's largest bf16
+//               logit (lowest column on ties); each CTA folds its tiles in
+//               shared memory and publishes one 64-bit key per token with a
+//               device-scope atomic max, and the last CTA to finish writes
+//               the chosen columns and clears the keys for the next call.
 //   fused only: warps 2-9 first quantise, in the kernel prologue, the token
 //               rows of every K block this CTA will use into an activation
 //               cache in shared memory (E4M3 codes in the swizzled B-operand
@@ -73,7 +79,27 @@ struct GemmParams {
     int w_tiled;             // weights in the tiled layout (one contiguous 16 KB run per tile)
     int test_skip_unit;      // -1, or a unit whose stage the producer never fills
     unsigned long long timeout_ns;
+    // greedy token choice (token == nullptr: off)
+    int *token;                  // [M] chosen column per token
+    float *logit;                // [M] its logit, or nullptr
+    unsigned long long *best;    // workspace: [64] keys, zero between calls
+    unsigned *done;              // workspace: CTAs finished, zero between calls
 };
+
+// Order-preserving 32-bit key of a finite float (larger value, larger key;
+// +0 and -0 get the same key).  Key 0 is below every finite value.
+__device__ __forceinline__ uint32_t logit_key(float v)
+{
+    uint32_t b = __float_as_uint(v);
+    if (b == 0x80000000u)
+        b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
 template <int NPAD, int MODE> struct GemmCfg {
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "token tile");
@@ -130,6 +156,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(act_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
+    unsigned long long *cta_best = reinterpret_cast<unsigned long long *>(smem + 512); // [64] greedy keys
     const int S = p.stages;
     uint8_t *ring = smem + C::kHeader;
     uint8_t *act_cache = ring + S * C::kStageBytes;
@@ -165,6 +192,10 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
         mbar_init(act_ready, 1);
         *abort_flag = 0;
         *last_flag = 0;
+    }
+    if (threadIdx.x < 64)
+        cta_best[threadIdx.x] = 0ull;
+    if (threadIdx.x == 0) {
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -462,6 +493,28 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             const int tile_b = static_cast<int>((u0 + nunits - 1) / kg);
             const SplitPlan plan_a = make_plan(tile_a);
             const SplitPlan plan_b = tile_b != tile_a ? make_plan(tile_b) : plan_a;
+            // Final values of weight row n for every token: round to bf16,
+            // store Y (when asked for) and fold the greedy choice.
+            auto finish_row = [&](int n) {
+                const bool in_n = n < p.N;
+#pragma unroll
+                for (int m = 0; m < NPAD; ++m) {
+                    if (m < p.M) {
+                        const __nv_bfloat16 h = __float2bfloat16_rn(acc[m]);
+                        if (in_n && p.y != nullptr)
+                            p.y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(h);
+                        if (p.token != nullptr) {
+                            const uint32_t key = in_n ? logit_key(__bfloat162float(h)) : 0u;
+                            const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+                            const uint32_t nmin =
+                                __reduce_min_sync(0xffffffffu, key == kmax ? static_cast<uint32_t>(n) : 0xffffffffu);
+                            if (lane == 0)
+                                atomicMax(&cta_best[m],
+                                          (static_cast<unsigned long long>(kmax) << 32) | (0xffffffffu - nmin));
+                        }
+                    }
+                }
+            };
             for (int i = 0; i < nunits; ++i) {
                 if (i > 0) {
                     if (++kb == kg) {
@@ -527,13 +580,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const int n = tile * C::kTileRows + row;
                 const bool whole_tile = (seg_first_kb == 0) && (kb == kg - 1);
                 if (whole_tile) {
-                    if (n < p.N) {
-#pragma unroll
-                        for (int m = 0; m < NPAD; ++m)
-                            if (m < p.M)
-                                p.y[static_cast<long long>(m) * p.N + n] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-                    }
+                    finish_row(n);
                 } else {
                     // K-split tile: publish this CTA's partial, and the last
                     // contributor to arrive sums all of them in contributor order.
@@ -587,13 +634,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                                             acc[mc + q] += v[j][q];
                             }
                         }
-                        if (n < p.N) {
-#pragma unroll
-                            for (int m = 0; m < NPAD; ++m)
-                                if (m < p.M)
-                                    p.y[static_cast<long long>(m) * p.N + n] =
-                                        __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-                        }
+                        finish_row(n);
                         if (warp == 2 && lane == 0)
                             p.counters[tile] = 0u; // ready for the next call
                     }
@@ -602,6 +643,31 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
 #pragma unroll
                 for (int m = 0; m < NPAD; ++m)
                     acc[m] = 0.0f;
+            }
+            if (p.token != nullptr) {
+                // ---- greedy: publish this CTA's keys; the last CTA finishes
+                named_bar_sync(1, 32 * C::kEpiWarps); // every warp's shared-memory folds are done
+                if (warp == 2) {
+                    for (int m = lane; m < p.M; m += 32)
+                        atomicMax(&p.best[m], cta_best[m]);
+                    __threadfence();
+                    __syncwarp();
+                    unsigned prev = 0;
+                    if (lane == 0)
+                        prev = atomic_add_acq_rel_gpu(p.done, 1u);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    if (prev == static_cast<unsigned>(p.ctas - 1)) {
+                        __threadfence();
+                        for (int m = lane; m < p.M; m += 32) {
+                            const unsigned long long k = atomicExch(&p.best[m], 0ull); // read and clear
+                            p.token[m] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k));
+                            if (p.logit != nullptr)
+                                p.logit[m] = key_logit(static_cast<uint32_t>(k >> 32));
+                        }
+                        if (lane == 0)
+                            *p.done = 0u;
+                    }
+                }
             }
         }
     }

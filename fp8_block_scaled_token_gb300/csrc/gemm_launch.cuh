@@ -112,6 +112,10 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.w_tiled = tiled ? 1 : 0;
     p.test_skip_unit = L.test_skip_unit;
     p.timeout_ns = L.timeout_ns;
+    p.token = L.token;
+    p.logit = L.logit;
+    p.best = reinterpret_cast<unsigned long long *>(wsb + wl.greedy_off);
+    p.done = reinterpret_cast<unsigned *>(wsb + wl.greedy_off + 64 * 8);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), 1, 1);

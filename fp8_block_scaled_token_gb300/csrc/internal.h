@@ -38,12 +38,13 @@ inline int token_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 
 
 // Workspace layout shared by the GEMM launchers:
 //   [0, 256)                status word (+ padding)
-//   [256, 256 + C)          ntiles 32-bit arrival counters, C rounded up to 256
+//   [256, 1024)             greedy choice: 64 64-bit keys, then the CTA counter
+//   [1024, 1024 + C)        ntiles 32-bit arrival counters, C rounded up to 256
 //   slots                   2 * ctas slots of NPAD * 128 fp32 partials
 //   act, act_scale          M x K codes and M x K/128 scales, used only when the
 //                           fused entry point quantises in a separate kernel
 struct WorkspaceLayout {
-    size_t counters_off, slots_off, act_off, act_scale_off, total;
+    size_t greedy_off, counters_off, slots_off, act_off, act_scale_off, total;
 };
 WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad, int M, int K);
 
@@ -62,6 +63,8 @@ struct GemmLaunch {
     cudaStream_t stream;
     int test_skip_unit;       // -1 normally
     unsigned long long timeout_ns;
+    int *token;               // greedy choice per token, or nullptr (then y must be set)
+    float *logit;             // its logit, or nullptr
 };
 
 // Shape and SM count -> schedule; shared by launch and size queries.

@@ -194,6 +194,31 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx,
                                         unsigned flags, void *stream);
 
 /*
+ * The output layer with the greedy next-token choice fused into its epilogue
+ * [P2 "The output layer, which did run": the 248,320-wide output layer feeds
+ * the choice of the next token].  Computes Y exactly as
+ * fp8_blockscaled_gemm_fused (bitwise the same values) and, per token m:
+ *   token[m] = the column n < N of the largest bf16 value y[m][n], compared
+ *              as numbers (+0 equals -0); among equal values the lowest n;
+ *   logit[m] = that value as fp32 (a zero is reported as +0).
+ * Each CTA reduces the tiles it finishes while they are still in registers;
+ * the logits are never read back from memory.  The choice is deterministic:
+ * it depends only on Y, whose values are bitwise reproducible.
+ * y: bf16 [M][N] as fp8_blockscaled_gemm_fused, or NULL to skip storing the
+ *    logits.  token: int32 [M], 4-byte aligned (required).  logit: fp32 [M],
+ *    4-byte aligned, or NULL.  NaN logits (NaN inputs) are outside the
+ *    contract.  Workspace as fp8_blockscaled_gemm_fused (the same size query);
+ *    the library leaves its greedy keys and counter at zero after every call.
+ * Other arguments as fp8_blockscaled_gemm_fused.
+ */
+FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx,
+                                               const uint8_t *wq, const float *ws,
+                                               void *y, int M, int N, int K,
+                                               int32_t *token, float *logit,
+                                               void *workspace, size_t workspace_bytes,
+                                               unsigned flags, void *stream);
+
+/*
  * fp8_blockscaled_gemm_fused without a caller-provided workspace, for callers
  * that cannot allocate device memory (code running under a graph capture
  * that must not allocate, allocator-less embedded runtimes, hooks that run

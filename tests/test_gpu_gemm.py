@@ -223,3 +223,23 @@ def test_bf16_tiled_bitwise_equal(M, N, K):
     b = fb.bf16_gemm_ref(x, wt, n=N)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_column_shards_match_the_whole_layer():
+    """Column sharding (each GPU would hold a 128-row-aligned slice of W and
+    compute its own columns of Y, with no reduction between GPUs): slices
+    quantised on their own give the same codes and scales as the slice of the
+    whole matrix, and the concatenated outputs meet the same tolerance."""
+    M, N, K = 8, 5120, 5120
+    x_cpu, w_cpu = synth.activations(M, K, seed=61), synth.weights(N, K, seed=62, outlier_p=0.01)
+    x, w = x_cpu.cuda(), w_cpu.cuda()
+    wq, ws = fb.fp8_quant_weight_blocks(w)
+    cuts = [0, 1280, 2688, 4096, 5120]
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sq, ss = fb.fp8_quant_weight_blocks(w[a:b].contiguous())
+        assert torch.equal(sq, wq[a:b]) and torch.equal(ss, ws[a // 128:b // 128])
+        parts.append(fb.fp8_blockscaled_gemm_fused(x, sq, ss))
+    torch.cuda.synchronize()
+    ref = oracle_layer(x_cpu, w_cpu)
+    check_y(torch.cat(parts, dim=1), ref["y"], ref["bound"], "column shards")
