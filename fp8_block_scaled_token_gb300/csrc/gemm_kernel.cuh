@@ -79,7 +79,7 @@ struct GemmParams {
     int w_tiled;             // weights in the tiled layout (one contiguous 16 KB run per tile)
     int test_skip_unit;      // -1, or a unit whose stage the producer never fills
     unsigned long long timeout_ns;
-    // greedy token choice (token == nullptr: off)
+    // greedy token choice (kernels instantiated with GREEDY only)
     int *token;                  // [M] chosen column per token
     float *logit;                // [M] its logit, or nullptr
     unsigned long long *best;    // workspace: [64] keys, zero between calls
@@ -138,7 +138,9 @@ template <int NPAD, int MODE> struct GemmCfg {
     }
 };
 
-template <int NPAD, int MODE>
+// GREEDY: the greedy-choice epilogue is compiled in (a separate instantiation,
+// so the plain layer carries none of its code).
+template <int NPAD, int MODE, bool GREEDY>
 __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, MODE>::kMinBlocks)
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p)
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         const __nv_bfloat16 h = __float2bfloat16_rn(acc[m]);
                         if (in_n && p.y != nullptr)
                             p.y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(h);
-                        if (p.token != nullptr) {
+                        if constexpr (GREEDY) {
                             const uint32_t key = in_n ? logit_key(__bfloat162float(h)) : 0u;
                             const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
                             const uint32_t nmin =
@@ -644,7 +646,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 for (int m = 0; m < NPAD; ++m)
                     acc[m] = 0.0f;
             }
-            if (p.token != nullptr) {
+            if constexpr (GREEDY) {
                 // ---- greedy: publish this CTA's keys; the last CTA finishes
                 named_bar_sync(1, 32 * C::kEpiWarps); // every warp's shared-memory folds are done
                 if (warp == 2) {

@@ -43,12 +43,12 @@ template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stag
         stages = C::kMaxStages;
 }
 
-template <int NPAD, int MODE>
+template <int NPAD, int MODE, bool GREEDY>
 fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
 {
     using C = GemmCfg<NPAD, MODE>;
     static unsigned long long attr_done = 0;
-    auto kernel = gemm_small_m_kernel<NPAD, MODE>;
+    auto kernel = gemm_small_m_kernel<NPAD, MODE, GREEDY>;
     int stages = 0, act_chunks = 0;
     gemm_smem_plan<NPAD, MODE>(sh, stages, act_chunks);
     if (act_chunks < 0 || stages < 2)
@@ -151,20 +151,36 @@ template <int MODE> bool fused_cache_fits(const GemmShape &sh)
     return act_chunks >= 0 && stages >= 2;
 }
 
+template <int MODE, bool GREEDY>
+fp8bs_status launch_gemm_greedy(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
+{
+    switch (sh.npad) {
+    case 16:
+        return launch_gemm_npad<16, MODE, GREEDY>(L, dev, sh);
+    case 32:
+        return launch_gemm_npad<32, MODE, GREEDY>(L, dev, sh);
+    case 48:
+        return launch_gemm_npad<48, MODE, GREEDY>(L, dev, sh);
+    default:
+        return launch_gemm_npad<64, MODE, GREEDY>(L, dev, sh);
+    }
+}
+
+// The greedy instantiations compile in their own translation unit (gemm_greedy.cu).
+extern template fp8bs_status launch_gemm_greedy<kModeFp8, true>(const GemmLaunch &, const DeviceInfo &,
+                                                                const GemmShape &);
+extern template fp8bs_status launch_gemm_greedy<kModeFp8Fused, true>(const GemmLaunch &, const DeviceInfo &,
+                                                                     const GemmShape &);
+
 template <int MODE>
 fp8bs_status launch_gemm_mode(const GemmLaunch &L, const DeviceInfo &dev)
 {
     const GemmShape sh = gemm_shape(MODE, L.M, L.N, L.K, dev.sms);
-    switch (sh.npad) {
-    case 16:
-        return launch_gemm_npad<16, MODE>(L, dev, sh);
-    case 32:
-        return launch_gemm_npad<32, MODE>(L, dev, sh);
-    case 48:
-        return launch_gemm_npad<48, MODE>(L, dev, sh);
-    default:
-        return launch_gemm_npad<64, MODE>(L, dev, sh);
+    if constexpr (MODE != kModeBf16) {
+        if (L.token != nullptr)
+            return launch_gemm_greedy<MODE, true>(L, dev, sh);
     }
+    return launch_gemm_greedy<MODE, false>(L, dev, sh);
 }
 
 } // namespace fp8bs
