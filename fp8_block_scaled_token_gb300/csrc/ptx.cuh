@@ -53,13 +53,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// True once the phase with parity `parity` has completed.
+// True once the phase with parity `parity` has completed.  While the phase
+// is open the thread may be suspended for up to 2 us (it wakes when the phase
+// completes): spinning waiters would otherwise take issue slots from the
+// warps doing the work, including those of the other CTA sharing the SM
+// (measured on GB300: vocab layer 208.5 -> 198.2 us, MLP down 22.5 -> 22.0 us).
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 2000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
