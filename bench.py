@@ -463,7 +463,7 @@ def time_graph(fn, reps_inner, reps_outer, stream):
 PASS_SHAPES = ((5120, 5120), (34816, 5120), (5120, 17408), (7168, 5120))  # (N, K)
 
 
-def decode_pass(dev, stream, peak, Ms=(1, 2, 4, 8, 16, 32, 64)):
+def decode_pass(dev, stream, peak, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 512)):
     """One decode pass: 256 GEMMs cycling the four layer shapes, every one with
     its own weights (22.4 GB, seeds 100 + i), then the output layer; timed as
     one graph per token count M."""
@@ -495,8 +495,10 @@ def decode_pass(dev, stream, peak, Ms=(1, 2, 4, 8, 16, 32, 64)):
                                               n=N)
         us = time_graph(f, 1, 20, stream)
         b = sum(algorithmic_bytes(M, N, K) for N, K, _, _ in layers)
+        flops = sum(2.0 * M * N * K for N, K, _, _ in layers)
         rows.append({"workload": "decode_pass_257", "M": M, "ms": round(us / 1e3, 4),
-                     "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
+                     "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
+                     "TFLOP/s": round(flops / us / 1e6, 1)})
         print(json.dumps(rows[-1]), file=sys.stderr, flush=True)
         del xs, ys, work
     del layers
@@ -513,7 +515,8 @@ def sweep(args, dev):
     stream = torch.cuda.Stream(device=dev)
     out = []
     l2 = 126 * 1024 * 1024
-    for name, Ms in (("square_decode", (1, 8)), ("mlp_up", (8,)), ("mlp_down", (8,)), ("vocab", (1, 8))):
+    for name, Ms in (("square_decode", (1, 8, 64, 128, 256, 512)), ("mlp_up", (8,)), ("mlp_down", (8,)),
+                     ("vocab", (1, 8))):
         cfg = workload(name)
         N, K = cfg["N"], cfg["K"]
         R = max(1, min(32, math.ceil(4 * l2 / (N * K))))
@@ -533,7 +536,8 @@ def sweep(args, dev):
             us = time_graph(f, R, max(1, 400 // R), stream)
             b = algorithmic_bytes(M, N, K)
             out.append({"workload": name, "M": M, "N": N, "K": K, "us": round(us, 3),
-                        "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
+                        "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
+                        "TFLOP/s": round(2.0 * M * N * K / us / 1e6, 1)})
             print(json.dumps(out[-1]), file=sys.stderr, flush=True)
             if name == "vocab":
                 # the output layer with the greedy token choice fused, logits not stored

@@ -104,14 +104,14 @@ fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataTyp
     return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
 }
 
-WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad, int M, int K)
+WorkspaceLayout workspace_layout(const GemmShape &sh, int M, int K)
 {
     auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
     WorkspaceLayout w;
     w.greedy_off = 256;
     w.counters_off = 1024;
-    w.slots_off = w.counters_off + up256(static_cast<size_t>(ntiles) * 4);
-    w.act_off = w.slots_off + static_cast<size_t>(2) * ctas * npad * 128 * 4;
+    w.slots_off = w.counters_off + up256(static_cast<size_t>(sh.ttiles) * sh.ntiles * 4);
+    w.act_off = w.slots_off + (sh.split ? static_cast<size_t>(sh.ttiles) * 2 * sh.ctas * sh.npad * 128 * 4 : 0);
     w.act_scale_off = w.act_off + up256(static_cast<size_t>(M) * K);
     w.total = w.act_scale_off + up256(static_cast<size_t>(M) * (K / 128) * 4);
     return w;
@@ -123,8 +123,34 @@ GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
     s.kg = mode == 2 ? K / 64 : K / 128;
     s.ntiles = (N + 127) / 128;
     s.units = static_cast<long long>(s.ntiles) * s.kg;
-    s.ctas = plan_ctas(s.units, sms);
     s.npad = token_pad(M);
+    s.ttiles = 1;
+    s.split = true;
+    if (M <= 64) {
+        // Decode: the K dimension is split across every SM (stream-K).
+        s.ctas = plan_ctas(s.units, sms);
+        return s;
+    }
+    // Larger M: one CTA per (weight tile, token tile) over the whole K, no
+    // split and no exchange, with the widest token tile that still occupies
+    // at least half of the SMs (a second, mostly empty wave would cost more
+    // than the idle half); the token tiles of a weight tile read it from L2
+    // after the first.
+    for (int tt : {256, 128, 64, 32}) {
+        const int tiles_m = (M + tt - 1) / tt;
+        if (2 * static_cast<long long>(s.ntiles) * tiles_m >= sms) {
+            s.npad = tt;
+            s.ttiles = tiles_m;
+            s.ctas = s.ntiles;
+            s.split = false;
+            return s;
+        }
+    }
+    // Too few weight tiles for that: split K, with 128- or 256-token tiles
+    // (above 256 tokens two of them side by side, each on half of the SMs).
+    s.npad = M <= 128 ? 128 : 256;
+    s.ttiles = (M + s.npad - 1) / s.npad;
+    s.ctas = plan_ctas(s.units, s.ttiles > 1 ? sms / s.ttiles : sms);
     s.m = M;
     return s;
 }
@@ -141,7 +167,7 @@ fp8bs_status check_gemm_shape(int M, int N, int K, int kmult)
 {
     if (M < 1 || N < 1 || K < 1)
         return FP8BS_ERR_INVALID_ARG;
-    if (M > 64 || K % kmult != 0 || N > (1 << 30) || K > (1 << 30))
+    if (M > kMaxTokens || K % kmult != 0 || N > (1 << 30) || K > (1 << 30))
         return FP8BS_ERR_UNSUPPORTED_SHAPE;
     return FP8BS_OK;
 }
@@ -177,7 +203,7 @@ fp8bs_status gemm_workspace(int mode, int M, int N, int K, size_t *bytes)
     if (st != FP8BS_OK)
         return st;
     const GemmShape sh = gemm_shape(mode, M, N, K, dev.sms);
-    *bytes = workspace_layout(sh.ntiles, sh.ctas, sh.npad, M, K).total;
+    *bytes = workspace_layout(sh, M, K).total;
     return FP8BS_OK;
 }
 
@@ -188,7 +214,7 @@ fp8bs_status run_gemm(GemmLaunch &L)
     if (st != FP8BS_OK)
         return st;
     const GemmShape sh = gemm_shape(L.mode, L.M, L.N, L.K, dev.sms);
-    if (L.workspace_bytes < workspace_layout(sh.ntiles, sh.ctas, sh.npad, L.M, L.K).total)
+    if (L.workspace_bytes < workspace_layout(sh, L.M, L.K).total)
         return FP8BS_ERR_WORKSPACE_TOO_SMALL;
     switch (L.mode) {
     case 0:
@@ -212,7 +238,7 @@ const char *fp8bs_status_string(fp8bs_status status)
     case FP8BS_ERR_INVALID_ARG:
         return "invalid argument (null pointer, size below 1, ldx below K, or unknown flag/dtype)";
     case FP8BS_ERR_UNSUPPORTED_SHAPE:
-        return "unsupported shape (GEMM M must be 1..64; K must be a multiple of 128, or 64 for the bf16 GEMM)";
+        return "unsupported shape (GEMM M must be 1..512, 1..64 with the greedy choice; K must be a multiple of 128, or 64 for the bf16 GEMM)";
     case FP8BS_ERR_MISALIGNED:
         return "misaligned pointer or row stride";
     case FP8BS_ERR_WORKSPACE_TOO_SMALL:
@@ -373,6 +399,8 @@ fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx, const uin
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
+    if (M > 64)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE; // one greedy key per token, at most 64
     if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||

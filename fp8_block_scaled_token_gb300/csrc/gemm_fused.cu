@@ -11,7 +11,7 @@ fp8bs_status launch_gemm_fused(const GemmLaunch &L, const DeviceInfo &dev)
     const GemmShape sh = gemm_shape(kModeFp8Fused, L.M, L.N, L.K, dev.sms);
     if (fused_cache_fits<kModeFp8Fused>(sh))
         return launch_gemm_mode<kModeFp8Fused>(L, dev);
-    const WorkspaceLayout wl = workspace_layout(sh.ntiles, sh.ctas, sh.npad, L.M, L.K);
+    const WorkspaceLayout wl = workspace_layout(sh, L.M, L.K);
     uint8_t *aq = static_cast<uint8_t *>(L.workspace) + wl.act_off;
     float *as = reinterpret_cast<float *>(static_cast<uint8_t *>(L.workspace) + wl.act_scale_off);
     fp8bs_status st = launch_quant_act(L.a, L.M, L.K, L.lda, aq, as, (L.flags & FP8BS_FLAG_OVERLAP_PREV) != 0,

@@ -102,17 +102,18 @@ __device__ __forceinline__ float key_logit(uint32_t k)
 }
 
 template <int NPAD, int MODE> struct GemmCfg {
-    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "token tile");
+    static_assert((NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64) || NPAD == 128 || NPAD == 256, "token tile");
     static constexpr int kTileRows = 128;                   // weight rows per tile (MMA M)
     static constexpr int kRowBytes = 128;                   // K bytes per row per unit
     static constexpr int kChunkElems = MODE == kModeBf16 ? 64 : 128;
     static constexpr int kWBytes = kTileRows * kRowBytes;   // 16 KB
-    static constexpr int kBBytes = NPAD * kRowBytes;        // 2..8 KB token tile
+    static constexpr int kBBytes = NPAD * kRowBytes;        // 2..32 KB token tile
     static constexpr int kStageBytes = kWBytes + (MODE == kModeFp8Fused ? 0 : kBBytes);
     static constexpr int kMaxStages = 12;
-    static constexpr int kAcc = 4;
+    static constexpr int kAcc = NPAD == 256 ? 2 : 4;       // TMEM holds 512 fp32 columns
     static constexpr int kTmemNeed = kAcc * NPAD;
-    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
+    static constexpr int kTmemCols =
+        kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
     // Up to 16 tokens the non-fused kernels run two CTAs per SM (a ~100 KB
     // ring each): the next GEMM's CTA, launched early by programmatic
@@ -121,7 +122,12 @@ template <int NPAD, int MODE> struct GemmCfg {
     // 200 KB ring for every layer shape of the workloads at M <= 16, and
     // loses at M = 32 (and the wider accumulators of NPAD >= 48 would spill).
     static constexpr int kMinBlocks = (MODE != kModeFp8Fused && NPAD == 16) ? 2 : 1;
-    static constexpr int kEpiWarps = 4;
+    // A 256-token tile splits its columns over two groups of four epilogue
+    // warps, so a thread keeps at most 128 accumulators in registers.
+    static constexpr int kColGroups = NPAD > 128 ? 2 : 1;
+    static constexpr int kCols = NPAD / kColGroups;         // token columns per epilogue thread
+    static constexpr int kEpiWarps = 4 * kColGroups;
+    static constexpr int kSaRegs = (kCols + 31) / 32;       // token scales held per lane (pre-quantised)
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kHeader = 1024;                    // barriers and flags
     static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;
@@ -146,6 +152,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         const GemmParams p)
 {
     using C = GemmCfg<NPAD, MODE>;
+    static_assert(!GREEDY || NPAD <= 64, "the greedy choice keeps one key per token for at most 64 tokens");
+    static_assert(MODE != kModeFp8Fused || NPAD <= 64, "the fused cast serves at most 64 tokens");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -264,8 +272,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     if (i == p.test_skip_unit)
                         continue;
                     const int kb = static_cast<int>((u0 + i) % kg);
-                    tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb * C::kChunkElems, 0,
-                                pol_b);
+                    tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb * C::kChunkElems,
+                                static_cast<int>(blockIdx.y) * NPAD, pol_b);
                 }
             }
             // Per-unit state advances by increments: no divisions in this
@@ -285,8 +293,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     const int wy = p.w_tiled ? (tile * kg + kb) * C::kTileRows : tile * C::kTileRows;
                     tma_load_2d(ring + s * C::kStageBytes, &tm_w, &full[s], wx, wy, pol_w);
                     if (MODE != kModeFp8Fused)
-                        tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems, 0,
-                                    pol_b);
+                        tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems,
+                                    static_cast<int>(blockIdx.y) * NPAD, pol_b);
                     // keep the L2 prefetch kPrefetch units ahead of the ring, once
                     // the first ring pass has been requested
                     if (C::kPrefetch > 0 && i + 1 >= S)
@@ -466,9 +474,16 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             const int quarter = warp & 3;             // TMEM lanes this warp may read
             const int row = quarter * 32 + lane;      // weight row within the tile
             const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-            float acc[NPAD];
+            // This thread's token columns: col0.. of the token tile, tokens
+            // tok0.. of the layer; mcnt of them exist (may exceed kCols).
+            const int col0 = ((warp - 2) >> 2) * C::kCols;
+            const int tok0 = static_cast<int>(blockIdx.y) * NPAD + col0;
+            const int mcnt = p.M - tok0;
+            float *const slots_y = p.slots + static_cast<long long>(blockIdx.y) * 2 * p.ctas * (NPAD * 128);
+            unsigned *const counters_y = p.counters + static_cast<long long>(blockIdx.y) * p.ntiles;
+            float acc[C::kCols];
 #pragma unroll
-            for (int m = 0; m < NPAD; ++m)
+            for (int m = 0; m < C::kCols; ++m)
                 acc[m] = 0.0f;
             int accb = 0;
             uint32_t acc_ph = 0;
@@ -500,11 +515,11 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             auto finish_row = [&](int n) {
                 const bool in_n = n < p.N;
 #pragma unroll
-                for (int m = 0; m < NPAD; ++m) {
-                    if (m < p.M) {
+                for (int m = 0; m < C::kCols; ++m) {
+                    if (m < mcnt) {
                         const __nv_bfloat16 h = __float2bfloat16_rn(acc[m]);
                         if (in_n && p.y != nullptr)
-                            p.y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(h);
+                            p.y[static_cast<long long>(tok0 + m) * p.N + n] = __bfloat16_as_ushort(h);
                         if constexpr (GREEDY) {
                             const uint32_t key = in_n ? logit_key(__bfloat162float(h)) : 0u;
                             const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
@@ -531,29 +546,35 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 if (seg_start)
                     seg_first_kb = kb;
                 if (MODE != kModeBf16 || seg_end) {
-                    float sw = 1.0f, sa0 = 0.0f, sa1 = 0.0f;
+                    float sw = 1.0f, sa_r[C::kSaRegs];
                     if (MODE != kModeBf16)
                         sw = p.ws[static_cast<long long>(tile) * kg + kb];
-                    if (MODE == kModeFp8) {
-                        if (lane < p.M)
-                            sa0 = p.as[static_cast<long long>(lane) * kg + kb];
-                        if (lane + 32 < p.M)
-                            sa1 = p.as[static_cast<long long>(lane + 32) * kg + kb];
+#pragma unroll
+                    for (int r = 0; r < C::kSaRegs; ++r) {
+                        sa_r[r] = 0.0f;
+                        if (MODE == kModeFp8 && r * 32 + lane < mcnt)
+                            sa_r[r] = p.as[static_cast<long long>(tok0 + r * 32 + lane) * kg + kb];
                     }
-                    const float *sa_c = act_scale + (MODE == kModeFp8Fused ? slot * NPAD : 0);
+                    const float *sa_c = act_scale + (MODE == kModeFp8Fused ? slot * NPAD : 0) + col0;
                     mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
                     named_bar_sync(1, 32 * C::kEpiWarps);
                     if (*abort_flag)
-                        break; // uniform across the four epilogue warps
+                        break; // uniform across the epilogue warps
                     tc_fence_after_sync();
-                    const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD);
+                    const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD + col0);
+                    // 32 columns per TMEM load and wait where the tile has them
+                    constexpr int kLd = (C::kCols % 32 == 0 && C::kColGroups == 1) ? 32 : 16;
+                    static_assert(C::kCols % kLd == 0, "whole loads only");
 #pragma unroll
-                    for (int c = 0; c < NPAD / 16; ++c) {
-                        uint32_t r[16];
-                        tmem_load16(taddr + c * 16, r);
+                    for (int c = 0; c < C::kCols / kLd; ++c) {
+                        uint32_t r[kLd];
+                        if constexpr (kLd == 32)
+                            tmem_load32(taddr + c * kLd, r);
+                        else
+                            tmem_load16(taddr + c * kLd, r);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = c * 16 + j;
+                        for (int j = 0; j < kLd; ++j) {
+                            const int m = c * kLd + j;
                             const float d = __uint_as_float(r[j]);
                             if (MODE == kModeBf16) {
                                 acc[m] = d;
@@ -562,7 +583,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                                 if (MODE == kModeFp8Fused)
                                     sam = sa_c[m];
                                 else
-                                    sam = __shfl_sync(0xffffffffu, m < 32 ? sa0 : sa1, m & 31);
+                                    sam = __shfl_sync(0xffffffffu, sa_r[m >> 5], m & 31);
                                 acc[m] = fmaf(sw * sam, d, acc[m]);
                             }
                         }
@@ -589,45 +610,45 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     const SplitPlan &pl = tile == tile_a ? plan_a : plan_b;
                     const int c_first = pl.c_first, c_last = pl.c_last;
                     auto slot_of = [&](int c) { return c == c_first ? pl.slot_first : 2 * c; };
-                    float *mine = p.slots + static_cast<long long>(slot_of(cta)) * (NPAD * 128);
+                    float *mine = slots_y + static_cast<long long>(slot_of(cta)) * (NPAD * 128) + col0 * 128;
 #pragma unroll
-                    for (int m = 0; m < NPAD; ++m)
-                        if (m < p.M)
+                    for (int m = 0; m < C::kCols; ++m)
+                        if (m < mcnt)
                             __stcg(mine + m * 128 + row, acc[m]);
                     named_bar_sync(1, 32 * C::kEpiWarps);
                     if (warp == 2 && lane == 0) {
                         // one release for the whole epilogue group's stores (ordered
                         // by the barrier above); acquire for the others' partials
-                        const unsigned prev = atomic_add_acq_rel_gpu(&p.counters[tile], 1u);
+                        const unsigned prev = atomic_add_acq_rel_gpu(&counters_y[tile], 1u);
                         *last_flag = (prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
                     }
                     named_bar_sync(1, 32 * C::kEpiWarps);
                     if (*last_flag) {
 #pragma unroll
-                        for (int m = 0; m < NPAD; ++m)
+                        for (int m = 0; m < C::kCols; ++m)
                             acc[m] = 0.0f;
                         // Issue every contributor's loads for a chunk of tokens at
                         // once (one L2 round trip per chunk), then add them in
                         // contributor order.
-                        constexpr int kMaxC = 6;
+                        constexpr int kMaxC = NPAD > 64 ? 2 : 6;
                         constexpr int kMC = NPAD <= 16 ? 16 : 8;
                         for (int c0 = c_first; c0 <= c_last; c0 += kMaxC) {
                             const int nc = c_last - c0 + 1 < kMaxC ? c_last - c0 + 1 : kMaxC;
                             const float *src[kMaxC];
 #pragma unroll
                             for (int j = 0; j < kMaxC; ++j)
-                                src[j] = p.slots + static_cast<long long>(slot_of(c0 + (j < nc ? j : 0))) * (NPAD * 128) +
-                                         row;
+                                src[j] = slots_y + static_cast<long long>(slot_of(c0 + (j < nc ? j : 0))) * (NPAD * 128) +
+                                         col0 * 128 + row;
 #pragma unroll
-                            for (int mc = 0; mc < NPAD; mc += kMC) {
-                                if (mc >= p.M)
+                            for (int mc = 0; mc < C::kCols; mc += kMC) {
+                                if (mc >= mcnt)
                                     break;
                                 float v[kMaxC][kMC];
 #pragma unroll
                                 for (int j = 0; j < kMaxC; ++j)
 #pragma unroll
                                     for (int q = 0; q < kMC; ++q)
-                                        v[j][q] = (j < nc && mc + q < p.M) ? __ldcg(src[j] + (mc + q) * 128) : 0.0f;
+                                        v[j][q] = (j < nc && mc + q < mcnt) ? __ldcg(src[j] + (mc + q) * 128) : 0.0f;
 #pragma unroll
                                 for (int j = 0; j < kMaxC; ++j)
 #pragma unroll
@@ -638,12 +659,12 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         }
                         finish_row(n);
                         if (warp == 2 && lane == 0)
-                            p.counters[tile] = 0u; // ready for the next call
+                            counters_y[tile] = 0u; // ready for the next call
                     }
                     named_bar_sync(1, 32 * C::kEpiWarps);
                 }
 #pragma unroll
-                for (int m = 0; m < NPAD; ++m)
+                for (int m = 0; m < C::kCols; ++m)
                     acc[m] = 0.0f;
             }
             if constexpr (GREEDY) {

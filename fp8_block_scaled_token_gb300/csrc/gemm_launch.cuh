@@ -88,7 +88,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     if (st != FP8BS_OK)
         return st;
 
-    const WorkspaceLayout wl = workspace_layout(sh.ntiles, sh.ctas, NPAD, L.M, L.K);
+    const WorkspaceLayout wl = workspace_layout(sh, L.M, L.K);
     uint8_t *wsb = static_cast<uint8_t *>(L.workspace);
     GemmParams p;
     p.M = L.M;
@@ -118,7 +118,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.done = reinterpret_cast<unsigned *>(wsb + wl.greedy_off + 64 * 8);
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), static_cast<unsigned>(sh.ttiles), 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = L.stream;
@@ -134,6 +134,8 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
 template <int MODE> bool fused_cache_fits(const GemmShape &sh)
 {
     int stages = 0, act_chunks = 0;
+    if (sh.m > 64 || sh.ttiles > 1)
+        return false; // the prologue cast serves one token tile of at most 64
     switch (sh.npad) {
     case 16:
         gemm_smem_plan<16, MODE>(sh, stages, act_chunks);
@@ -154,6 +156,14 @@ template <int MODE> bool fused_cache_fits(const GemmShape &sh)
 template <int MODE, bool GREEDY>
 fp8bs_status launch_gemm_greedy(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
 {
+    // 128- and 256-token tiles exist for the plain (non-fused, non-greedy)
+    // GEMMs only; the callers reject larger M before they get here.
+    if constexpr (MODE != kModeFp8Fused && !GREEDY) {
+        if (sh.npad == 128)
+            return launch_gemm_npad<128, MODE, GREEDY>(L, dev, sh);
+        if (sh.npad == 256)
+            return launch_gemm_npad<256, MODE, GREEDY>(L, dev, sh);
+    }
     switch (sh.npad) {
     case 16:
         return launch_gemm_npad<16, MODE, GREEDY>(L, dev, sh);
@@ -161,8 +171,10 @@ fp8bs_status launch_gemm_greedy(const GemmLaunch &L, const DeviceInfo &dev, cons
         return launch_gemm_npad<32, MODE, GREEDY>(L, dev, sh);
     case 48:
         return launch_gemm_npad<48, MODE, GREEDY>(L, dev, sh);
-    default:
+    case 64:
         return launch_gemm_npad<64, MODE, GREEDY>(L, dev, sh);
+    default:
+        return FP8BS_ERR_UNSUPPORTED_SHAPE;
     }
 }
 

@@ -33,20 +33,28 @@ fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataTyp
 
 fp8bs_status launch_status(cudaError_t e);
 
-// Token-tile width for M rows (16, 32, 48 or 64).
-inline int token_pad(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
+// Largest token count of the GEMMs.
+constexpr int kMaxTokens = 512;
+
+// Token-tile width for M <= 64 rows (16, 32, 48 or 64); gemm_shape picks the
+// tiles of larger M.
+inline int token_pad(int M)
+{
+    return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+}
 
 // Workspace layout shared by the GEMM launchers:
 //   [0, 256)                status word (+ padding)
 //   [256, 1024)             greedy choice: 64 64-bit keys, then the CTA counter
-//   [1024, 1024 + C)        ntiles 32-bit arrival counters, C rounded up to 256
-//   slots                   2 * ctas slots of NPAD * 128 fp32 partials
+//   [1024, 1024 + C)        ttiles * ntiles 32-bit arrival counters, C rounded up to 256
+//   slots                   ttiles * 2 * ctas slots of NPAD * 128 fp32 partials
 //   act, act_scale          M x K codes and M x K/128 scales, used only when the
 //                           fused entry point quantises in a separate kernel
 struct WorkspaceLayout {
     size_t greedy_off, counters_off, slots_off, act_off, act_scale_off, total;
 };
-WorkspaceLayout workspace_layout(int ntiles, int ctas, int npad, int M, int K);
+struct GemmShape;
+WorkspaceLayout workspace_layout(const GemmShape &sh, int M, int K);
 
 struct GemmLaunch {
     int mode;                 // GemmMode
@@ -70,6 +78,8 @@ struct GemmLaunch {
 // Shape and SM count -> schedule; shared by launch and size queries.
 struct GemmShape {
     int kg, ntiles, ctas, npad, m;
+    int ttiles; // token tiles (grid y)
+    bool split; // K is split across CTAs (exchange slots needed)
     long long units;
 };
 GemmShape gemm_shape(int mode, int M, int N, int K, int sms);

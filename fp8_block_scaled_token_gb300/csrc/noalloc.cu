@@ -53,7 +53,7 @@ extern "C" fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ld
         return st;
     constexpr int kFused = 1; // the fused mode of the GEMM kernel
     const GemmShape sh = gemm_shape(kFused, M, N, K, dev.sms);
-    const WorkspaceLayout wl = workspace_layout(sh.ntiles, sh.ctas, sh.npad, M, K);
+    const WorkspaceLayout wl = workspace_layout(sh, M, K);
     if (wl.total > kNoallocScratchBytes)
         return FP8BS_ERR_UNSUPPORTED_SHAPE; // needs more scratch than the library holds
 

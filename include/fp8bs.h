@@ -4,7 +4,7 @@
  *     Y[M,N] = dequant(Aq[M,K]) . dequant(Wq[N,K])^T
  *
  * on one GB300 (sm_103a).  M is 1..64 rows (decode / speculative-verify
- * batches), W is E4M3 with one fp32 scale per 128x128 block, the activations
+ * batches; up to 512 for chunked prefill), W is E4M3 with one fp32 scale per 128x128 block, the activations
  * are cast on the fly to E4M3 with one fp32 scale per token per 128 K.
  *
  * Sources (page title, section):
@@ -160,7 +160,13 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, 
  * aq: u8 [M][K], 16-byte aligned.   as: fp32 [M][K/128].
  * wq: u8 [N][K], 16-byte aligned.   ws: fp32 [ceil(N/128)][K/128].
  * y : bf16 [M][N], 2-byte aligned.
- * 1 <= M <= 64, N >= 1, K >= 128, K % 128 == 0.
+ * 1 <= M <= 512, N >= 1, K >= 128, K % 128 == 0.  Up to 64 tokens the
+ * token tile is 16, 32, 48 or 64 wide; 65..128 tokens use one 128-wide tile,
+ * 129..256 one 256-wide tile, and 257..512 two 256-wide tiles that run side by
+ * side on half of the SMs each (the larger-M, chunked-prefill regime, where
+ * the pages note that the work turns from memory- to compute-bound:
+ * "Kernel-Level Optimisations for LLM Inference and Training", "Start with
+ * the bound").
  * workspace: device, 256-byte aligned, >= fp8_blockscaled_gemm_workspace_size.
  * flags: any of FP8BS_FLAG_OVERLAP_PREV, FP8BS_FLAG_WEIGHTS_TILED (then wq is
  * in the tiled layout of fp8_quant_weight_blocks_tiled).
@@ -209,6 +215,7 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx,
  *    4-byte aligned, or NULL.  NaN logits (NaN inputs) are outside the
  *    contract.  Workspace as fp8_blockscaled_gemm_fused (the same size query);
  *    the library leaves its greedy keys and counter at zero after every call.
+ * 1 <= M <= 64 (FP8BS_ERR_UNSUPPORTED_SHAPE above).
  * Other arguments as fp8_blockscaled_gemm_fused.
  */
 FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx,
@@ -248,7 +255,7 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ldx
  * Same swap-AB / TMA / split-K pipeline with bf16 tensor-core MMAs and no
  * block scales.
  * x: bf16 [M][K], w: bf16 [N][K], both 16-byte aligned; y: bf16 [M][N].
- * 1 <= M <= 64, N >= 1, K >= 64, K % 64 == 0.
+ * 1 <= M <= 512, N >= 1, K >= 64, K % 64 == 0.
  */
 FP8BS_API fp8bs_status bf16_gemm_ref_workspace_size(int M, int N, int K, size_t *bytes);
 /*

@@ -85,7 +85,7 @@ def test_gemm_validation(L):
     g = L.fp8_blockscaled_gemm
     assert g(NUL, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == INVALID
     assert g(A16, A16, A16, A16, A16, 0, 256, 512, A16, 1 << 20, 0, S) == INVALID
-    assert g(A16, A16, A16, A16, A16, 65, 256, 512, A16, 1 << 20, 0, S) == SHAPE
+    assert g(A16, A16, A16, A16, A16, 513, 256, 512, A16, 1 << 20, 0, S) == SHAPE     # M above 512
     assert g(A16, A16, A16, A16, A16, 8, 256, 520, A16, 1 << 20, 0, S) == SHAPE
     assert g(A16, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 4, S) == INVALID
     assert g(A1, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == MISALIGNED
@@ -93,6 +93,9 @@ def test_gemm_validation(L):
     f = L.fp8_blockscaled_gemm_fused
     assert f(A16, 100, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == INVALID           # ldx < K
     assert f(A16, 516, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == MISALIGNED        # ldx % 8
+    gr = L.fp8_blockscaled_gemm_fused_greedy
+    assert gr(A16, 512, A16, A16, A16, 65, 256, 512, A16, NUL, A16, 1 << 20, 0, S) == SHAPE  # greedy: M <= 64
+    assert gr(A16, 512, A16, A16, A16, 8, 256, 512, NUL, NUL, A16, 1 << 20, 0, S) == INVALID  # token required
     b = L.bf16_gemm_ref
     assert b(A16, A16, A16, 8, 256, 96, A16, 1 << 20, 0, S) == SHAPE                         # K % 64
     assert b(A16, A16, A16, 64, 256, 128, A16, 1 << 20, 0, S) != SHAPE
