@@ -33,7 +33,8 @@
 //               weights only, and the MMA reads its B operand from the cache.
 //
 // Shared memory: [1 KB barriers and flags][ring: S stages][activation cache]
-// [activation scales]; S and the cache size are chosen per launch.
+// [activation scales][scale products]; S and the cache size are chosen per
+// launch.
 //
 // Every wait is bounded; on time-out the CTA records a code in the status
 // word, drains what it has in flight, frees its tensor memory and returns.
@@ -127,7 +128,13 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kColGroups = NPAD > 128 ? 2 : 1;
     static constexpr int kCols = NPAD / kColGroups;         // token columns per epilogue thread
     static constexpr int kEpiWarps = 4 * kColGroups;
-    static constexpr int kSaRegs = (kCols + 31) / 32;       // token scales held per lane (pre-quantised)
+    // From 32 tokens up, the per-unit scale products s_w * s_a[m] are formed
+    // once per token and read back from shared memory (four per load), which
+    // removes a shuffle and a multiply per token per weight row.  The 16-token
+    // tile (decode) keeps the per-lane scales and shuffles: there the extra
+    // shared-memory round trip on the per-unit critical path cost ~0.2 us.
+    static constexpr bool kProducts = NPAD >= 32 && MODE != kModeBf16;
+    static constexpr int kProdBytes = kProducts ? 2 * NPAD * 4 : 0; // double-buffered
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kHeader = 1024;                    // barriers and flags
     static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;
@@ -140,7 +147,7 @@ template <int NPAD, int MODE> struct GemmCfg {
     // Dynamic shared memory of a launch (+1024 for aligning the base).
     static constexpr int smem_bytes(int stages, int act_chunks)
     {
-        return 1024 + kHeader + stages * kStageBytes + act_chunks * (kBBytes + kActScaleBytes);
+        return 1024 + kHeader + stages * kStageBytes + act_chunks * (kBBytes + kActScaleBytes) + kProdBytes;
     }
 };
 
@@ -171,6 +178,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     uint8_t *ring = smem + C::kHeader;
     uint8_t *act_cache = ring + S * C::kStageBytes;
     float *act_scale = reinterpret_cast<float *>(act_cache + p.act_chunks * C::kBBytes);
+    float *prod = act_scale + p.act_chunks * NPAD; // [2][NPAD] s_w * s_a of the current units
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -532,6 +540,21 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     }
                 }
             };
+            // Scales of the next unit to promote, loaded one unit ahead by
+            // the thread of each token (thread index tpr < NPAD).
+            const int tpr = threadIdx.x - 64;
+            float nx_sw = 0.0f, nx_sa = 0.0f;
+            auto load_scales = [&](int tl, int kbb, int sl) {
+                nx_sw = p.ws[static_cast<long long>(tl) * kg + kbb];
+                if (MODE == kModeFp8) {
+                    const int tok = static_cast<int>(blockIdx.y) * NPAD + tpr;
+                    nx_sa = tok < p.M ? p.as[static_cast<long long>(tok) * kg + kbb] : 0.0f;
+                } else {
+                    nx_sa = act_scale[sl * NPAD + tpr]; // zero for rows >= M
+                }
+            };
+            if (C::kProducts && tpr < NPAD && nunits > 0)
+                load_scales(tile, kb, slot);
             for (int i = 0; i < nunits; ++i) {
                 if (i > 0) {
                     if (++kb == kg) {
@@ -546,14 +569,27 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 if (seg_start)
                     seg_first_kb = kb;
                 if (MODE != kModeBf16 || seg_end) {
-                    float sw = 1.0f, sa_r[C::kSaRegs];
-                    if (MODE != kModeBf16)
+                    // One thread per token forms s_w * s_a for this unit from
+                    // the scales it loaded one unit ahead, and loads the next
+                    // unit's; the barrier below publishes the products
+                    // (double-buffered by unit parity: a buffer is rewritten
+                    // only after every thread has passed the next unit's
+                    // barrier).
+                    float *pr = prod + (i & 1) * NPAD;
+                    if (C::kProducts && tpr < NPAD) {
+                        pr[tpr] = nx_sw * nx_sa;
+                        if (i + 1 < nunits) {
+                            const bool wrap = kb + 1 == kg;
+                            load_scales(wrap ? tile + 1 : tile, wrap ? 0 : kb + 1, slot + 1 == kg ? 0 : slot + 1);
+                        }
+                    }
+                    // 16-token tile: each lane holds the scale of token `lane`
+                    // (pre-quantised) and shuffles it to the others.
+                    float sw = 1.0f, sa_l = 0.0f;
+                    if constexpr (!C::kProducts && MODE != kModeBf16) {
                         sw = p.ws[static_cast<long long>(tile) * kg + kb];
-#pragma unroll
-                    for (int r = 0; r < C::kSaRegs; ++r) {
-                        sa_r[r] = 0.0f;
-                        if (MODE == kModeFp8 && r * 32 + lane < mcnt)
-                            sa_r[r] = p.as[static_cast<long long>(tok0 + r * 32 + lane) * kg + kb];
+                        if (MODE == kModeFp8 && lane < mcnt)
+                            sa_l = p.as[static_cast<long long>(tok0 + lane) * kg + kb];
                     }
                     const float *sa_c = act_scale + (MODE == kModeFp8Fused ? slot * NPAD : 0) + col0;
                     mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
@@ -572,20 +608,26 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                             tmem_load32(taddr + c * kLd, r);
                         else
                             tmem_load16(taddr + c * kLd, r);
+                        float sc[kLd];
+                        if constexpr (C::kProducts) {
+#pragma unroll
+                            for (int q = 0; q < kLd / 4; ++q)
+                                *reinterpret_cast<float4 *>(&sc[4 * q]) =
+                                    reinterpret_cast<const float4 *>(pr + col0 + c * kLd)[q];
+                        } else if constexpr (MODE != kModeBf16) {
+#pragma unroll
+                            for (int j = 0; j < kLd; ++j)
+                                sc[j] = sw * (MODE == kModeFp8Fused ? sa_c[c * kLd + j]
+                                                                    : __shfl_sync(0xffffffffu, sa_l, (c * kLd + j) & 31));
+                        }
 #pragma unroll
                         for (int j = 0; j < kLd; ++j) {
                             const int m = c * kLd + j;
                             const float d = __uint_as_float(r[j]);
-                            if (MODE == kModeBf16) {
+                            if (MODE == kModeBf16)
                                 acc[m] = d;
-                            } else {
-                                float sam;
-                                if (MODE == kModeFp8Fused)
-                                    sam = sa_c[m];
-                                else
-                                    sam = __shfl_sync(0xffffffffu, sa_r[m >> 5], m & 31);
-                                acc[m] = fmaf(sw * sam, d, acc[m]);
-                            }
+                            else
+                                acc[m] = fmaf(sc[j], d, acc[m]);
                         }
                     }
                     tc_fence_before_sync();
