@@ -156,13 +156,11 @@ template <int MODE> bool fused_cache_fits(const GemmShape &sh)
 template <int MODE, bool GREEDY>
 fp8bs_status launch_gemm_greedy(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
 {
-    // 128- and 256-token tiles exist for the plain (non-fused, non-greedy)
-    // GEMMs only; the callers reject larger M before they get here.
+    // 128-token tiles exist for the plain (non-fused, non-greedy) GEMMs only;
+    // the callers reject larger M before they get here.
     if constexpr (MODE != kModeFp8Fused && !GREEDY) {
         if (sh.npad == 128)
             return launch_gemm_npad<128, MODE, GREEDY>(L, dev, sh);
-        if (sh.npad == 256)
-            return launch_gemm_npad<256, MODE, GREEDY>(L, dev, sh);
     }
     switch (sh.npad) {
     case 16:

@@ -161,12 +161,13 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, 
  * wq: u8 [N][K], 16-byte aligned.   ws: fp32 [ceil(N/128)][K/128].
  * y : bf16 [M][N], 2-byte aligned.
  * 1 <= M <= 512, N >= 1, K >= 128, K % 128 == 0.  Up to 64 tokens the
- * token tile is 16, 32, 48 or 64 wide; 65..128 tokens use one 128-wide tile,
- * 129..256 one 256-wide tile, and 257..512 two 256-wide tiles that run side by
- * side on half of the SMs each (the larger-M, chunked-prefill regime, where
- * the pages note that the work turns from memory- to compute-bound:
- * "Kernel-Level Optimisations for LLM Inference and Training", "Start with
- * the bound").
+ * token tile is 16, 32, 48 or 64 wide and K is split across every SM; above
+ * 64 tokens (the larger-M, chunked-prefill regime, where the pages note that
+ * the work turns from memory- to compute-bound: "Kernel-Level Optimisations
+ * for LLM Inference and Training", "Start with the bound") the tokens are
+ * cut into tiles of up to 128 and each CTA computes one 128-row weight tile
+ * for one token tile over the whole K, splitting K only when N is too small
+ * to occupy half of the SMs that way.
  * workspace: device, 256-byte aligned, >= fp8_blockscaled_gemm_workspace_size.
  * flags: any of FP8BS_FLAG_OVERLAP_PREV, FP8BS_FLAG_WEIGHTS_TILED (then wq is
  * in the tiled layout of fp8_quant_weight_blocks_tiled).
