@@ -111,7 +111,7 @@ WorkspaceLayout workspace_layout(const GemmShape &sh, int M, int K)
     w.greedy_off = 256;
     w.counters_off = 1024;
     w.slots_off = w.counters_off + up256(static_cast<size_t>(sh.ttiles) * sh.ntiles * 4);
-    w.act_off = w.slots_off + (sh.split ? static_cast<size_t>(sh.ttiles) * 2 * sh.ctas * sh.npad * 128 * 4 : 0);
+    w.act_off = w.slots_off + (sh.split ? static_cast<size_t>(2) * sh.ctas * sh.npad * 128 * 4 : 0);
     w.act_scale_off = w.act_off + up256(static_cast<size_t>(M) * K);
     w.total = w.act_scale_off + up256(static_cast<size_t>(M) * (K / 128) * 4);
     return w;
@@ -131,28 +131,41 @@ GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
         s.ctas = plan_ctas(s.units, sms);
         return s;
     }
-    // Larger M: one CTA per (weight tile, token tile) over the whole K, no
-    // split and no exchange, with the widest token tile (at most 128) that
-    // still occupies at least half of the SMs; the token tiles of a weight
-    // tile read it from L2 after the first.  (256-token tiles promote 15%
-    // slower per token than 128-token ones, enough that several 128-token
-    // waves beat one 256-token wave: square layer M = 512 68.0 -> 56.6 us,
-    // MLP up M = 512 251.8 -> 218.1 us.)
+    // Larger M.  The work units are (token tile, weight tile, K block), the
+    // K block fastest.  With at least as many (token tile, weight tile) pairs
+    // of 128 tokens as SMs, stream-K over all of them: every CTA gets the
+    // same number of units and shares at most the two pairs at its ends.
+    {
+        const int tiles_m = (M + 127) / 128;
+        if (static_cast<long long>(s.ntiles) * tiles_m >= sms) {
+            s.npad = 128;
+            s.ttiles = tiles_m;
+            s.units = static_cast<long long>(s.ntiles) * tiles_m * s.kg;
+            s.ctas = plan_ctas(s.units, sms);
+            return s;
+        }
+    }
+    // Fewer pairs than SMs: one CTA per pair over the whole K, no split and
+    // no exchange, with the widest token tile (at most 128) whose pairs still
+    // occupy at least half of the SMs; the token tiles of a weight tile read
+    // it from L2 after the first.  (256-token tiles promote 15% slower per
+    // token than 128-token ones and are not used.)
     for (int tt : {128, 64, 32}) {
         const int tiles_m = (M + tt - 1) / tt;
         if (2 * static_cast<long long>(s.ntiles) * tiles_m >= sms) {
             s.npad = tt;
             s.ttiles = tiles_m;
-            s.ctas = s.ntiles;
+            s.units = static_cast<long long>(s.ntiles) * tiles_m * s.kg;
+            s.ctas = s.ntiles * tiles_m; // one pair per CTA
             s.split = false;
             return s;
         }
     }
-    // Too few weight tiles for that: split K, with 128-token tiles side by
-    // side, each on its share of the SMs.
+    // Too few weight tiles for that: stream-K over 128-token pairs.
     s.npad = 128;
     s.ttiles = (M + 127) / 128;
-    s.ctas = plan_ctas(s.units, sms / s.ttiles > 0 ? sms / s.ttiles : 1);
+    s.units = static_cast<long long>(s.ntiles) * s.ttiles * s.kg;
+    s.ctas = plan_ctas(s.units, sms);
     s.m = M;
     return s;
 }

@@ -69,8 +69,9 @@ enum GemmMode : int {
 struct GemmParams {
     int M, N, K;
     int kg;          // K blocks per tile (K/128 for FP8, K/64 for bf16)
-    int ntiles;      // ceil(N / 128)
-    long long units; // ntiles * kg
+    int ntiles;      // ceil(N / 128) weight tiles
+    long long units; // token tiles * ntiles * kg: unit u is K block u % kg of
+                     // pair u / kg = (token tile, weight tile), weight tile fastest
     int ctas;
     int stages;      // ring depth, <= kMaxStages
     int act_chunks;  // fused: K blocks in the activation cache (>= distinct K blocks of any CTA)
@@ -167,6 +168,10 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     using C = GemmCfg<NPAD, MODE>;
     static_assert(!GREEDY || NPAD <= 64, "the greedy choice keeps one key per token for at most 64 tokens");
     static_assert(MODE != kModeFp8Fused || NPAD <= 64, "the fused cast serves at most 64 tokens");
+    // Instantiations that only ever run one token tile (the 16-token decode
+    // tile, the fused cast and the greedy choice serve at most 64 tokens):
+    // pair index == weight tile, and no token-tile stepping is compiled in.
+    constexpr bool kOneTT = NPAD == 16 || MODE == kModeFp8Fused || GREEDY;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -196,11 +201,13 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     // activation-cache slot of its i-th unit is i mod kg.
     const int kb0 = static_cast<int>(u0 % kg);
     // TMA coordinates of the weight tile of unit u: (K offset, row) in the
-    // row-major matrix, or (0, u*128) in the tiled layout where the tiles of
-    // consecutive units are consecutive 16 KB runs.
+    // row-major matrix, or (0, (weight tile * kg + kb) * 128) in the tiled
+    // layout where the tiles of consecutive K blocks are consecutive 16 KB
+    // runs (used by the optional L2 prefetch; the loops below step instead).
     auto w_x = [&](long long u) { return p.w_tiled ? 0 : static_cast<int>(u % kg) * C::kChunkElems; };
     auto w_y = [&](long long u) {
-        return p.w_tiled ? static_cast<int>(u * C::kTileRows) : static_cast<int>(u / kg) * C::kTileRows;
+        const int wt = static_cast<int>((u / kg) % p.ntiles);
+        return p.w_tiled ? (wt * kg + static_cast<int>(u % kg)) * C::kTileRows : wt * C::kTileRows;
     };
 
     if (threadIdx.x == 0) {
@@ -269,33 +276,47 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     }
                 }
             };
+            // Per-unit state (K block, weight tile, first token row) advances
+            // by increments from the CTA's first unit: no divisions in these
+            // single-thread loops, whose latency sets the issue rate.
+            const int pair_first = static_cast<int>(u0 / kg);
+            const int wt_first = kOneTT ? pair_first : pair_first % p.ntiles;
+            const int trow_first = kOneTT ? 0 : (pair_first / p.ntiles) * NPAD;
+            int kb = kb0, wt = wt_first, trow = trow_first;
+            auto step = [&](int &k, int &w, int &t) {
+                if (++k == kg) {
+                    k = 0;
+                    ++w;
+                    if (!kOneTT && w == p.ntiles) {
+                        w = 0;
+                        t += NPAD;
+                    }
+                }
+            };
             // Weights for the first ring pass, possibly before the previous grid is done.
-            for (int i = 0; i < pre; ++i) {
+            for (int i = 0; i < pre; ++i, step(kb, wt, trow)) {
                 if (i == p.test_skip_unit)
                     continue;
-                const long long u = u0 + i;
                 mbar_arrive_expect_tx(&full[i], tx);
                 armed_mask |= 1u << i;
-                tma_load_2d(ring + i * C::kStageBytes, &tm_w, &full[i], w_x(u), w_y(u), pol_w);
+                const int wx = p.w_tiled ? 0 : kb * C::kChunkElems;
+                const int wy = p.w_tiled ? (wt * kg + kb) * C::kTileRows : wt * C::kTileRows;
+                tma_load_2d(ring + i * C::kStageBytes, &tm_w, &full[i], wx, wy, pol_w);
             }
             prefetch_upto(pre + C::kPrefetch);
             grid_dependency_wait();
             weights_readable = true; // the previous grid has completed
             if (MODE != kModeFp8Fused) {
-                for (int i = 0; i < pre; ++i) {
+                int kb_b = kb0, wt_b = wt_first, trow_b = trow_first;
+                for (int i = 0; i < pre; ++i, step(kb_b, wt_b, trow_b)) {
                     if (i == p.test_skip_unit)
                         continue;
-                    const int kb = static_cast<int>((u0 + i) % kg);
-                    tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb * C::kChunkElems,
-                                static_cast<int>(blockIdx.y) * NPAD, pol_b);
+                    tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb_b * C::kChunkElems,
+                                trow_b, pol_b);
                 }
             }
-            // Per-unit state advances by increments: no divisions in this
-            // single-thread loop, whose latency sets the issue rate.
             int s = pre % S;
             uint32_t ph = static_cast<uint32_t>(pre / S) & 1u;
-            int kb = static_cast<int>((u0 + pre) % kg);
-            int tile = static_cast<int>((u0 + pre) / kg);
             for (int i = pre; i < nunits; ++i) {
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutProducer, p.timeout_ns))
                     break;
@@ -304,11 +325,11 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     armed_mask |= 1u << s;
                     armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
                     const int wx = p.w_tiled ? 0 : kb * C::kChunkElems;
-                    const int wy = p.w_tiled ? (tile * kg + kb) * C::kTileRows : tile * C::kTileRows;
+                    const int wy = p.w_tiled ? (wt * kg + kb) * C::kTileRows : wt * C::kTileRows;
                     tma_load_2d(ring + s * C::kStageBytes, &tm_w, &full[s], wx, wy, pol_w);
                     if (MODE != kModeFp8Fused)
                         tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems,
-                                    static_cast<int>(blockIdx.y) * NPAD, pol_b);
+                                    trow, pol_b);
                     // keep the L2 prefetch kPrefetch units ahead of the ring, once
                     // the first ring pass has been requested
                     if (C::kPrefetch > 0 && i + 1 >= S)
@@ -318,10 +339,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     s = 0;
                     ph ^= 1u;
                 }
-                if (++kb == kg) {
-                    kb = 0;
-                    ++tile;
-                }
+                step(kb, wt, trow);
             }
             // Nothing may still be landing in shared memory when the CTA exits:
             // wait (bounded) for the last phase armed on every stage.
@@ -489,12 +507,15 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             const int row = quarter * 32 + lane;      // weight row within the tile
             const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
             // This thread's token columns: col0.. of the token tile, tokens
-            // tok0.. of the layer; mcnt of them exist (may exceed kCols).
+            // tok0.. of the layer (per pair); mcnt of them exist (may exceed kCols).
             const int col0 = ((warp - 2) >> 2) * C::kCols;
-            const int tok0 = static_cast<int>(blockIdx.y) * NPAD + col0;
-            const int mcnt = p.M - tok0;
-            float *const slots_y = p.slots + static_cast<long long>(blockIdx.y) * 2 * p.ctas * (NPAD * 128);
-            unsigned *const counters_y = p.counters + static_cast<long long>(blockIdx.y) * p.ntiles;
+            const int pair_start = static_cast<int>(u0 / kg);
+            int wt = kOneTT ? pair_start : pair_start % p.ntiles;  // weight tile
+            int ttile = kOneTT ? 0 : pair_start / p.ntiles;        // token tile
+            int tok0 = ttile * NPAD + col0;
+            int mcnt = p.M - tok0;
+            float *const slots_y = p.slots;
+            unsigned *const counters_y = p.counters;
             float acc[C::kCols];
 #pragma unroll
             for (int m = 0; m < C::kCols; ++m)
@@ -550,22 +571,29 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             // the thread of each token (thread index tpr < NPAD).
             const int tpr = threadIdx.x - 64;
             float nx_sw = 0.0f, nx_sa = 0.0f;
-            auto load_scales = [&](int tl, int kbb, int sl) {
-                nx_sw = p.ws[static_cast<long long>(tl) * kg + kbb];
+            auto load_scales = [&](int wtl, int ttl, int kbb, int sl) {
+                nx_sw = p.ws[static_cast<long long>(wtl) * kg + kbb];
                 if (MODE == kModeFp8) {
-                    const int tok = static_cast<int>(blockIdx.y) * NPAD + tpr;
+                    const int tok = ttl * NPAD + tpr;
                     nx_sa = tok < p.M ? p.as[static_cast<long long>(tok) * kg + kbb] : 0.0f;
                 } else {
                     nx_sa = act_scale[sl * NPAD + tpr]; // zero for rows >= M
                 }
             };
             if (C::kProducts && tpr < NPAD && nunits > 0)
-                load_scales(tile, kb, slot);
+                load_scales(wt, ttile, kb, slot);
             for (int i = 0; i < nunits; ++i) {
                 if (i > 0) {
                     if (++kb == kg) {
                         kb = 0;
                         ++tile;
+                        ++wt;
+                        if (!kOneTT && wt == p.ntiles) {
+                            wt = 0;
+                            ++ttile;
+                            tok0 += NPAD;
+                            mcnt -= NPAD;
+                        }
                     }
                     if (++slot == kg)
                         slot = 0;
@@ -586,14 +614,16 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         pr[tpr] = nx_sw * nx_sa;
                         if (i + 1 < nunits) {
                             const bool wrap = kb + 1 == kg;
-                            load_scales(wrap ? tile + 1 : tile, wrap ? 0 : kb + 1, slot + 1 == kg ? 0 : slot + 1);
+                            const bool wrap_w = !kOneTT && wrap && wt + 1 == p.ntiles;
+                            load_scales(wrap ? (wrap_w ? 0 : wt + 1) : wt, wrap_w ? ttile + 1 : ttile, wrap ? 0 : kb + 1,
+                                        slot + 1 == kg ? 0 : slot + 1);
                         }
                     }
                     // 16-token tile: each lane holds the scale of token `lane`
                     // (pre-quantised) and shuffles it to the others.
                     float sw = 1.0f, sa_l = 0.0f;
                     if constexpr (!C::kProducts && MODE != kModeBf16) {
-                        sw = p.ws[static_cast<long long>(tile) * kg + kb];
+                        sw = p.ws[static_cast<long long>(wt) * kg + kb];
                         if (MODE == kModeFp8 && lane < mcnt)
                             sa_l = p.as[static_cast<long long>(tok0 + lane) * kg + kb];
                     }
@@ -650,7 +680,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 if (!seg_end)
                     continue;
                 // ---- tile segment complete: store or reduce
-                const int n = tile * C::kTileRows + row;
+                const int n = wt * C::kTileRows + row;
                 const bool whole_tile = (seg_first_kb == 0) && (kb == kg - 1);
                 if (whole_tile) {
                     finish_row(n);
@@ -681,7 +711,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         // once (one L2 round trip per chunk), then add them in
                         // contributor order.
                         constexpr int kMaxC = NPAD > 64 ? 2 : 6;
-                        constexpr int kMC = NPAD <= 16 ? 16 : 8;
+                        constexpr int kMC = NPAD <= 16 ? 16 : NPAD > 64 ? 32 : 8;
                         for (int c0 = c_first; c0 <= c_last; c0 += kMaxC) {
                             const int nc = c_last - c0 + 1 < kMaxC ? c_last - c0 + 1 : kMaxC;
                             const float *src[kMaxC];

@@ -53,6 +53,8 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     gemm_smem_plan<NPAD, MODE>(sh, stages, act_chunks);
     if (act_chunks < 0 || stages < 2)
         return FP8BS_ERR_UNSUPPORTED_SHAPE; // not reached: the fused launcher checks first
+    if ((NPAD == 16 || MODE == kModeFp8Fused || GREEDY) && sh.ttiles != 1)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE; // not reached: these serve one token tile only
     const int smem = C::smem_bytes(stages, act_chunks);
     fp8bs_status st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), kSmemLimit, dev.device, &attr_done);
     if (st != FP8BS_OK)
@@ -60,8 +62,8 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
 
     CUtensorMap tm_w, tm_b;
     const bool tiled = (L.flags & FP8BS_FLAG_WEIGHTS_TILED) != 0;
-    // Tiled weights are addressed as a [units * 128 rows][128 bytes] matrix.
-    const uint64_t tiled_rows = static_cast<uint64_t>(sh.units) * 128;
+    // Tiled weights are addressed as a [ntiles * kg * 128 rows][128 bytes] matrix.
+    const uint64_t tiled_rows = static_cast<uint64_t>(sh.ntiles) * sh.kg * 128;
     if (MODE == kModeBf16) {
         if (tiled)
             st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, tiled_rows, 64, 128, 64, 128);
@@ -118,7 +120,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.done = reinterpret_cast<unsigned *>(wsb + wl.greedy_off + 64 * 8);
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), static_cast<unsigned>(sh.ttiles), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), 1, 1);
     cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = L.stream;
