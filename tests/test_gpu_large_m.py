@@ -1,7 +1,7 @@
-"""The larger-M regime (65..512 tokens, chunked-prefill-like): 128- and
-256-wide token tiles, and two 256-wide token tiles side by side above 256
-tokens.  Same numeric contract and oracle as the decode path: codes and
-scales bit-exact, Y within the layer's tolerance, bitwise reproducible."""
+"""The larger-M regime (65..512 tokens, chunked-prefill-like): token tiles of
+up to 128, one CTA per (token tile, weight tile) pair or stream-K over the
+pairs.  Same numeric contract and oracle as the decode path: codes and scales
+bit-exact, Y within the layer's tolerance, bitwise reproducible."""
 import numpy as np
 import pytest
 import torch
@@ -73,9 +73,6 @@ def test_deterministic_tiled_and_counters():
         assert torch.equal(again.view(torch.int16), first.view(torch.int16))
     torch.cuda.synchronize()
     assert not work[:1024].any(), "status word and greedy area must stay clear"
-    # every arrival counter (both token tiles) back at zero
-    ntiles = (N + 127) // 128
-    assert not work[1024:1024 + 2 * ntiles * 4].any()
 
 
 def test_bf16_gemm_large_m():
@@ -96,3 +93,34 @@ def test_limits():
     x513 = synth.activations(513, 512, seed=742, device="cuda")
     with pytest.raises(fb.Fp8bsError):
         fb.fp8_blockscaled_gemm_fused(x513, wq, ws)              # at most 512 tokens
+
+
+def test_pair_stream_k_every_pair_split():
+    """152 (token tile, weight tile) pairs of two K blocks each: stream-K over
+    the pairs gives every CTA two units, so every pair is shared by two CTAs
+    and goes through the exchange."""
+    M, N, K = 512, 128 * 38, 256
+    x_cpu = synth.activations(M, K, seed=750, outlier_p=0.001)
+    w_cpu = synth.weights(N, K, seed=751, outlier_p=0.01)
+    x, w = x_cpu.cuda(), w_cpu.cuda()
+    wq, ws = fb.fp8_quant_weight_blocks(w, tiled=True)
+    work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K))
+    y = fb.fp8_blockscaled_gemm_fused(x, wq, ws, workspace=work, n=N)
+    torch.cuda.synchronize()
+    ref = oracle_layer(x_cpu, w_cpu)
+    check_y(y, ref["y"], ref["bound"], "pairs M=%d N=%d K=%d" % (M, N, K))
+    again = fb.fp8_blockscaled_gemm_fused(x, wq, ws, workspace=work, n=N, flags=fb.FLAG_OVERLAP_PREV)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), y.view(torch.int16))
+    ntiles, ttiles = N // 128, (M + 127) // 128
+    assert not work[:1024 + ntiles * ttiles * 4].any(), "status, greedy area and counters back at zero"
+
+
+def test_square_m512_bitwise_over_10_runs():
+    x = synth.activations(512, 5120, seed=760, device="cuda")
+    wq, ws = fb.fp8_quant_weight_blocks(synth.weights(5120, 5120, seed=761, device="cuda"), tiled=True)
+    work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(512, 5120, 5120))
+    first = fb.fp8_blockscaled_gemm_fused(x, wq, ws, workspace=work, n=5120)
+    for _ in range(9):
+        again = fb.fp8_blockscaled_gemm_fused(x, wq, ws, workspace=work, n=5120, flags=fb.FLAG_OVERLAP_PREV)
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
