@@ -59,6 +59,8 @@ def lib():
         "fp8bs_workspace_status": [vp, i, ctypes.POINTER(i)],
         "fp8bs_split_plan": [i, i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(ctypes.c_longlong),
                              ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)],
+        "fp8bs_gemm_schedule": [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
+                                ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(i)],
         "fp8bs_testhook_gemm_stall": [vp, vp, vp, vp, vp, i, i, i, vp, sz, i, ctypes.c_ulonglong, vp],
     }
     for name, args in sigs.items():
@@ -321,3 +323,10 @@ def split_plan(N, K, bf16=False, num_sms=0, cta=-1):
     _check("fp8bs_split_plan", lib().fp8bs_split_plan(N, K, 1 if bf16 else 0, num_sms, cta, ctypes.byref(c),
                                                       ctypes.byref(u), ctypes.byref(b), ctypes.byref(e)))
     return c.value, u.value, (b.value if cta >= 0 else None), (e.value if cta >= 0 else None)
+
+
+def gemm_schedule(M, N, K, num_sms=0):
+    """dict(npad, token_tiles, ctas, units, split) the FP8 GEMMs use for M tokens."""
+    v = [ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_longlong(0), ctypes.c_int(0)]
+    _check("fp8bs_gemm_schedule", lib().fp8bs_gemm_schedule(M, N, K, num_sms, *[ctypes.byref(a) for a in v]))
+    return dict(npad=v[0].value, token_tiles=v[1].value, ctas=v[2].value, units=v[3].value, split=bool(v[4].value))

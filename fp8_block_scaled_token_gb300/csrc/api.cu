@@ -521,6 +521,31 @@ fp8bs_status fp8bs_split_plan(int N, int K, int bf16, int num_sms, int cta, int 
     return FP8BS_OK;
 }
 
+fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int *npad, int *token_tiles, int *ctas,
+                                 long long *units, int *split)
+{
+    if (!npad || !token_tiles || !ctas || !units || !split)
+        return FP8BS_ERR_INVALID_ARG;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    int sms = num_sms;
+    if (sms <= 0) {
+        DeviceInfo dev;
+        st = current_device(&dev);
+        if (st != FP8BS_OK)
+            return st;
+        sms = dev.sms;
+    }
+    const GemmShape sh = gemm_shape(0, M, N, K, sms);
+    *npad = sh.npad;
+    *token_tiles = sh.ttiles;
+    *ctas = sh.ctas;
+    *units = sh.units;
+    *split = sh.split ? 1 : 0;
+    return FP8BS_OK;
+}
+
 } // extern "C"
 
 // Test hook (declared in include/fp8bs_testing.h): the FP8 GEMM with the

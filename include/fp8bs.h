@@ -283,6 +283,19 @@ FP8BS_API fp8bs_status bf16_gemm_ref(const void *x, const void *w, void *y,
 FP8BS_API fp8bs_status fp8bs_workspace_status(const void *workspace, int clear, int *code);
 
 /*
+ * The schedule the FP8 GEMMs choose for M tokens (the plan above is its
+ * M <= 64 case), exposed for inspection and tests.  Writes the token-tile
+ * width (*npad), the number of token tiles, the CTA count, the work-unit
+ * count (units = token tiles * ceil(N/128) * K/128, the K block fastest,
+ * then the 128-row weight tile) and whether K is split across CTAs
+ * (*split = 1: the fixed-order exchange runs; 0: every CTA owns whole
+ * (token tile, weight tile) pairs).  num_sms <= 0 means "the current
+ * device".  Nothing is launched.
+ */
+FP8BS_API fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int *npad, int *token_tiles,
+                                           int *ctas, long long *units, int *split);
+
+/*
  * The K-split schedule the GEMMs use, exposed for inspection and tests.
  * Work unit = (128-row weight tile, 128-wide K block) [(tile, 64-wide K
  * block) for bf16_gemm_ref, bf16 = 1]; units are ordered tile-major and

@@ -129,3 +129,34 @@ def test_split_plan_partitions_units(L):
             contrib = [c for c, v in partial_tiles.items() if t in v]
             if contrib:
                 assert contrib == list(range(contrib[0], contrib[-1] + 1))
+
+
+def test_gemm_schedule_policy(L):
+    """The schedule for M tokens: up to 64 tokens one token tile and K split
+    over every SM; above, whole (token tile, weight tile) pairs per CTA when
+    they occupy at least half of the SMs, stream-K over 128-token pairs
+    otherwise (when the pairs cover every SM, or when N is too small)."""
+    def tpad(M):
+        return 16 if M <= 16 else 32 if M <= 32 else 48 if M <= 48 else 64
+    for sms in (152, 148, 160):
+        for M in (1, 8, 16, 17, 33, 64, 65, 100, 128, 129, 256, 300, 384, 512):
+            for N, K in ((5120, 5120), (34816, 5120), (5120, 17408), (640, 1024), (300, 256), (128, 128)):
+                s = fb.gemm_schedule(M, N, K, sms)
+                ntiles, kg = (N + 127) // 128, K // 128
+                assert s["units"] == s["token_tiles"] * ntiles * kg
+                assert s["token_tiles"] == (M + s["npad"] - 1) // s["npad"]
+                if M <= 64:
+                    assert (s["npad"], s["token_tiles"], s["split"]) == (tpad(M), 1, True)
+                    assert s["ctas"] == min(s["units"], sms)
+                elif not s["split"]:
+                    assert s["npad"] in (32, 64, 128)
+                    assert s["ctas"] == s["token_tiles"] * ntiles and 2 * s["ctas"] >= sms
+                    assert ntiles * ((M + 127) // 128) < sms, "pairs cover the SMs: stream-K expected"
+                else:
+                    assert s["npad"] == 128 and s["ctas"] == min(s["units"], sms)
+    sq = lambda M: fb.gemm_schedule(M, 5120, 5120, 152)
+    assert sq(512) == dict(npad=128, token_tiles=4, ctas=152, units=6400, split=True)
+    assert sq(256) == dict(npad=128, token_tiles=2, ctas=80, units=3200, split=False)
+    assert sq(8) == dict(npad=16, token_tiles=1, ctas=152, units=1600, split=True)
+    with pytest.raises(fb.Fp8bsError):
+        fb.gemm_schedule(513, 5120, 5120, 152)
