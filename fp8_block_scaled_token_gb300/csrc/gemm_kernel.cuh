@@ -6,19 +6,23 @@
 // pipeline for the 16-bit output-layer baseline ("The profiler said the kernel
 // ran zero times", "The output layer, which did run").
 //
-// Design (one CTA per SM, warp-specialised):
+// Work is cut into units of one 128-wide K block of one (token tile, weight
+// tile) pair; each CTA takes a contiguous range of units (stream-K), so a
+// pair may be split across CTAs and is then summed in a fixed order.
+//
+// Design (warp-specialised; two CTAs per SM for the 16-token tile):
 //   warp 0      TMA producer: streams 128-row x 128-byte weight tiles (and,
 //               when the activations are pre-quantised or bf16, the token
 //               tile of the same K block) into an S-stage shared-memory ring,
 //               128-byte swizzled, no multicast.
 //   warp 1      MMA issuer: per 128-wide K block, four tcgen05.mma with the
 //               weights as the 128-row A operand and the tokens (padded to
-//               NPAD = 16/32/48/64) as the B operand, fp32 accumulator in
+//               NPAD = 16/32/48/64/128) as the B operand, fp32 accumulator in
 //               tensor memory (4 buffers so the epilogue never stalls it).
 //   warps 2-5   promotion / epilogue: one thread per weight row reads its
 //               accumulator row (tcgen05.ld), multiplies by
 //               s_w[tile,kb] * s_a[m,kb] and adds into fp32 registers; at the
-//               end of a tile it stores bf16 Y, or hands its partial to the
+//               end of a pair it stores bf16 Y, or hands its partial to the
 //               fixed-order K-split reduction.
 //   greedy (optional, the output layer): while storing a finished tile the
 //               epilogue warps also pick, per token, the tile's largest bf16
@@ -47,10 +51,6 @@
 #include "ptx.cuh"
 #include "quant_math.cuh"
 
-// L2 prefetch depth (units beyond the ring); a tuning knob, off by default.
-#ifndef FP8BS_PREFETCH_UNITS
-#define FP8BS_PREFETCH_UNITS 0
-#endif
 
 // Columns per TMEM load-and-wait in the promotion step: 64 for the 128-token
 // tile (measured: square layer M = 256 31.2 -> 29.5 us), 32 where the
@@ -144,7 +144,6 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kProdBytes = kProducts ? 2 * NPAD * 4 : 0; // double-buffered
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kHeader = 1024;                    // barriers and flags
-    static constexpr int kPrefetch = FP8BS_PREFETCH_UNITS;
     static constexpr int kMmaSteps = kRowBytes / 32;        // 32 bytes of K per tcgen05.mma
     static constexpr int kActScaleBytes = NPAD * 4;         // per cached K block
     static constexpr uint32_t kIdesc =
@@ -200,15 +199,6 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     // The CTA's units cover the cyclic run of K blocks starting at kb0; the
     // activation-cache slot of its i-th unit is i mod kg.
     const int kb0 = static_cast<int>(u0 % kg);
-    // TMA coordinates of the weight tile of unit u: (K offset, row) in the
-    // row-major matrix, or (0, (weight tile * kg + kb) * 128) in the tiled
-    // layout where the tiles of consecutive K blocks are consecutive 16 KB
-    // runs (used by the optional L2 prefetch; the loops below step instead).
-    auto w_x = [&](long long u) { return p.w_tiled ? 0 : static_cast<int>(u % kg) * C::kChunkElems; };
-    auto w_y = [&](long long u) {
-        const int wt = static_cast<int>((u / kg) % p.ntiles);
-        return p.w_tiled ? (wt * kg + static_cast<int>(u % kg)) * C::kTileRows : wt * C::kTileRows;
-    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -261,21 +251,6 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             const uint32_t tx = C::kStageBytes;
             uint32_t armed_mask = 0, armed_parity = 0;
             const int pre = p.prefetch_before_wait ? (nunits < S ? nunits : S) : 0;
-            // Units beyond the first ring pass go to L2 ahead of time (once the
-            // weights may be read: before the dependency wait only with the
-            // overlap flag).
-            int prefetched = S;
-            bool weights_readable = p.prefetch_before_wait != 0;
-            auto prefetch_upto = [&](int limit) {
-                if constexpr (C::kPrefetch > 0) {
-                    if (!weights_readable)
-                        return;
-                    for (; prefetched < limit && prefetched < nunits; ++prefetched) {
-                        const long long u = u0 + prefetched;
-                        tma_prefetch_l2_2d(&tm_w, w_x(u), w_y(u));
-                    }
-                }
-            };
             // Per-unit state (K block, weight tile, first token row) advances
             // by increments from the CTA's first unit: no divisions in these
             // single-thread loops, whose latency sets the issue rate.
@@ -303,9 +278,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const int wy = p.w_tiled ? (wt * kg + kb) * C::kTileRows : wt * C::kTileRows;
                 tma_load_2d(ring + i * C::kStageBytes, &tm_w, &full[i], wx, wy, pol_w);
             }
-            prefetch_upto(pre + C::kPrefetch);
             grid_dependency_wait();
-            weights_readable = true; // the previous grid has completed
             if (MODE != kModeFp8Fused) {
                 int kb_b = kb0, wt_b = wt_first, trow_b = trow_first;
                 for (int i = 0; i < pre; ++i, step(kb_b, wt_b, trow_b)) {
@@ -330,10 +303,6 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     if (MODE != kModeFp8Fused)
                         tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems,
                                     trow, pol_b);
-                    // keep the L2 prefetch kPrefetch units ahead of the ring, once
-                    // the first ring pass has been requested
-                    if (C::kPrefetch > 0 && i + 1 >= S)
-                        prefetch_upto(i + 1 + C::kPrefetch);
                 }
                 if (++s == S) {
                     s = 0;

@@ -136,16 +136,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
-// Bring a 2-D tile into L2 only (no shared memory, no completion tracking):
-// lets the producer keep many more bytes in flight than its ring holds.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // Fetch the 128-byte line holding `p` into this SM's L1 (no result).
 __device__ __forceinline__ void prefetch_l1(const void *p)
 {
