@@ -33,6 +33,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -114,10 +115,11 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, out_dir=None):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_%s.csv" % str(index).replace("/", "_"))
+        base = out_dir or tempfile.mkdtemp(prefix="fp8bs_clocks_")
+        self.path = os.path.join(base, "clocks_%s.csv" % str(index).replace("/", "_"))
 
     def start(self):
         try:
@@ -314,7 +316,7 @@ def run_ours(args, world, rank, local):
     if fb.workspace_status(work) != 0:
         raise RuntimeError("device-side timeout during warm-up")
 
-    clocks = ClockSampler(gpu_query_id(dev))
+    clocks = ClockSampler(gpu_query_id(dev), args.out_dir)
     clocks.start()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -573,9 +575,10 @@ def sweep(args, dev):
         out.append({"workload": "vocab_bf16", "M": M, "N": N, "K": K, "us": round(us, 3),
                     "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
         print(json.dumps(out[-1]), file=sys.stderr, flush=True)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    with open(os.path.join(ROOT, "gpurun_out", "bench_configs.json"), "w") as fh:
-        json.dump(out, fh, indent=1)
+    if args.out_dir:
+        os.makedirs(args.out_dir, exist_ok=True)
+        with open(os.path.join(args.out_dir, "bench_configs.json"), "w") as fh:
+            json.dump(out, fh, indent=1)
 
 
 # ---------------------------------------------------------------- reference arm: the CPU oracle
@@ -623,6 +626,8 @@ def main(argv=None):
     ap.add_argument("--configs", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out-dir", default=None,
+                    help="directory for the clock samples and the --configs table (default: a temporary one)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
