@@ -160,3 +160,21 @@ def test_gemm_schedule_policy(L):
     assert sq(8) == dict(npad=16, token_tiles=1, ctas=152, units=1600, split=True)
     with pytest.raises(fb.Fp8bsError):
         fb.gemm_schedule(513, 5120, 5120, 152)
+
+
+def test_c_caller_compiles_and_runs(L, tmp_path):
+    """A plain C program, compiled with the system C compiler against the
+    header and linked with the library, runs the host-side calls."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "abi_from_c")
+    libdir = os.path.dirname(fb.LIB_PATH)
+    src = os.path.join(ROOT, "tests", "c", "abi_from_c.c")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", exe,
+                        "-L", libdir, "-lfp8bs", "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
