@@ -242,7 +242,7 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx,
  * call shares the one array, so calls that can overlap on the GPU (different
  * streams without ordering) race and must not be issued.  Device-side
  * time-outs are recorded in the shared array and are not reported back.
- * Arguments and result as fp8_blockscaled_gemm_fused.
+ * Arguments and result as fp8_blockscaled_gemm_fused, with 1 <= M <= 64.
  */
 FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ldx,
                                                 const uint8_t *wq, const float *ws,
