@@ -22,6 +22,10 @@ What each function follows is stated in ``oracle.c``.  In brief:
   128-wide K block, with the error-bound reference sum |a||w|.
 * ``gemm_bf16`` -- the 16-bit output-layer product of the same page, fp64.
 * ``round_bf16`` -- one fp64 -> bf16 rounding, nearest-even.
+* ``mx_quant`` / ``mx_gemm`` -- the microscaling (MX) variant of the layer:
+  E4M3 elements with one power-of-two scale per 32 values along K, the
+  conversion of the OCP microscaling specification (the pages only name the
+  MX formats, "Kernel-Level Optimisations for LLM Inference and Training").
 * ``greedy`` -- the greedy next-token choice the output layer feeds ("The
   profiler said the kernel ran zero times", section "The output layer, which
   did run"): per token, the column of the largest bf16 logit, lowest column on
@@ -85,6 +89,10 @@ class Oracle:
         L.oracle_gemm_bf16.restype = _int
         L.oracle_gemm_bf16.argtypes = [_u16p, _u16p, _int, _int, _int,
                                        _i32p, _int, _f64p, _f64p, _int]
+        L.oracle_mx_quant.restype = _int
+        L.oracle_mx_quant.argtypes = [ctypes.c_void_p, _int, _int, _int, _u8p, _u8p]
+        L.oracle_mx_gemm.restype = _int
+        L.oracle_mx_gemm.argtypes = [_u8p, _u8p, _u8p, _u8p, _int, _int, _int, _i32p, _int, _f64p, _f64p, _int]
         L.oracle_greedy.restype = _int
         L.oracle_greedy.argtypes = [_u16p, _int, _int, _int, _i32p, _f32p]
         self.lib = L
@@ -226,6 +234,50 @@ class Oracle:
         return {"xq": xq, "xs": xs, "wq": wq, "ws": ws, "y": y, "bound": bound}
 
 
+    # -- MX (microscaling) E4M3 -------------------------------------------------
+    def mx_quant(self, x):
+        """1x32 power-of-two block quantisation along K (the OCP microscaling
+        conversion).  x: float32 [rows, K], or uint16 bf16 bit patterns.
+        Returns (codes uint8 [rows, K], scale bytes uint8 [rows, K/32]; the
+        scale of a block is 2^(byte - 127))."""
+        x = np.ascontiguousarray(x)
+        if x.dtype == np.float32:
+            dtype = 0
+        elif x.dtype == np.uint16:
+            dtype = 1
+        else:
+            raise TypeError("x must be float32 or bf16 bit patterns (uint16)")
+        rows, K = x.shape
+        codes = np.empty((rows, K), dtype=np.uint8)
+        sb = np.empty((rows, K // 32 if K % 32 == 0 else 0), dtype=np.uint8)
+        rc = self.lib.oracle_mx_quant(x.ctypes.data_as(ctypes.c_void_p), dtype, rows, K,
+                                      _ptr(codes, ctypes.c_uint8), _ptr(sb, ctypes.c_uint8))
+        if rc != 0:
+            raise ValueError("oracle_mx_quant: bad shape or non-finite input")
+        return codes, sb
+
+    def mx_gemm(self, aq, as_bytes, wq, ws_bytes, cols=None, nthreads=None):
+        """fp64 product of two MX operands: aq [M,K] / as_bytes [M,K/32] and
+        wq [N,K] / ws_bytes [N,K/32].  Returns (y, bound) [M, ncols]."""
+        aq = np.ascontiguousarray(aq, dtype=np.uint8)
+        asb = np.ascontiguousarray(as_bytes, dtype=np.uint8)
+        wq = np.ascontiguousarray(wq, dtype=np.uint8)
+        wsb = np.ascontiguousarray(ws_bytes, dtype=np.uint8)
+        M, K = aq.shape
+        N = wq.shape[0]
+        if wq.shape[1] != K:
+            raise ValueError("K mismatch")
+        c, ncols, cptr = self._cols(cols, N)
+        y = np.empty((M, ncols), dtype=np.float64)
+        bound = np.empty((M, ncols), dtype=np.float64)
+        rc = self.lib.oracle_mx_gemm(_ptr(aq, ctypes.c_uint8), _ptr(asb, ctypes.c_uint8),
+                                     _ptr(wq, ctypes.c_uint8), _ptr(wsb, ctypes.c_uint8), M, N, K, cptr, ncols,
+                                     _ptr(y, ctypes.c_double), _ptr(bound, ctypes.c_double),
+                                     nthreads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle_mx_gemm: bad arguments")
+        return y, bound
+
     # -- greedy token choice ----------------------------------------------------
     def greedy(self, y_bf16_bits, N=None):
         """Per token row of bf16 logits (uint16 bit patterns [M, ldy]): the
@@ -263,6 +315,7 @@ def mutant(n: int) -> Oracle:
 def __getattr__(name):
     # Module-level shortcuts: oracle.quant_act(...) == oracle.default().quant_act(...)
     if name in ("e4m3_decode_table", "e4m3_encode", "round_bf16", "f32_to_bf16_bits",
-                "quant_act", "quant_weight", "gemm_fp8", "gemm_bf16", "linear_fp8", "greedy"):
+                "quant_act", "quant_weight", "gemm_fp8", "gemm_bf16", "linear_fp8", "greedy",
+                "mx_quant", "mx_gemm"):
         return getattr(default(), name)
     raise AttributeError(name)

@@ -274,6 +274,9 @@ typedef struct {
     /* bf16 GEMM operands */
     const uint16_t *xb;
     const uint16_t *wb;
+    /* MX GEMM scale bytes (codes in aq / wq) */
+    const uint8_t *as8;
+    const uint8_t *ws8;
     int M, N, K;
     const int *cols;   /* optional list of output columns */
     int ncols;
@@ -349,7 +352,37 @@ static void bf16_columns(gemm_job *g)
     }
 }
 
+/* MX product: 32-wide blocks, scale 2^(byte - 127) per block and operand. */
+static void mx_columns(gemm_job *g)
+{
+    int kb32 = g->K / 32;
+    for (int j = g->j0; j < g->j1; ++j) {
+        int n = g->cols ? g->cols[j] : j;
+        const uint8_t *wrow = g->wq + (size_t)n * g->K;
+        const uint8_t *wsc = g->ws8 + (size_t)n * kb32;
+        for (int m = 0; m < g->M; ++m) {
+            const uint8_t *arow = g->aq + (size_t)m * g->K;
+            const uint8_t *asc = g->as8 + (size_t)m * kb32;
+            double y = 0.0, bound = 0.0;
+            for (int b = 0; b < kb32; ++b) {
+                double p = 0.0, pabs = 0.0;
+                for (int k = b * 32; k < b * 32 + 32; ++k) {
+                    double prod = g->table[arow[k]] * g->table[wrow[k]];
+                    p += prod;
+                    pabs += fabs(prod);
+                }
+                double sc = ldexp(1.0, (int)asc[b] - 127 + (int)wsc[b] - 127);
+                y += sc * p;
+                bound += sc * pabs;
+            }
+            g->y[(size_t)m * g->ncols + j] = y;
+            g->bound[(size_t)m * g->ncols + j] = bound;
+        }
+    }
+}
+
 static void *fp8_worker(void *p) { fp8_columns((gemm_job *)p); return NULL; }
+static void *mx_worker(void *p) { mx_columns((gemm_job *)p); return NULL; }
 static void *bf16_worker(void *p) { bf16_columns((gemm_job *)p); return NULL; }
 
 /* Split the output columns over nthreads workers.  Each output element is
@@ -485,4 +518,89 @@ int oracle_greedy(const uint16_t *y, int M, int N, int ldy, int32_t *token, floa
             logit[m] = bv == 0.0f ? 0.0f : bv;
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* MX (microscaling) E4M3: 32 consecutive values along K share one      */
+/* power-of-two scale stored as an 8-bit biased exponent (UE8M0).        */
+/* ------------------------------------------------------------------ */
+/* The pages only name the MX formats ("Kernel-Level Optimisations for LLM
+   Inference and Training", on CUTLASS).  Reading taken, the conversion of
+   the OCP Microscaling Formats specification: per block of 32 values, with
+   amax the largest magnitude, the shared exponent is
+   e = floor(log2(amax)) - 8 (8 = the exponent of E4M3's largest normal,
+   448 = 1.75 * 2^8), clamped to [-127, 127]; the scale is X = 2^e, stored as
+   the byte e + 127; each element is E4M3(v / X), nearest-even and
+   saturating at 448 (v / X is exact: X is a power of two).  A block of
+   zeros takes e = 0.  Input: rows x K values, fp32 (dtype 0) or bf16 bit
+   patterns (dtype 1), K % 32 == 0.  Output: codes [rows][K], scale bytes
+   [rows][K/32]. */
+int oracle_mx_quant(const void *x, int dtype, int rows, int K, uint8_t *codes, uint8_t *scale_bytes)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0 || (dtype != 0 && dtype != 1))
+        return -1;
+    for (int r = 0; r < rows; ++r) {
+        for (int b = 0; b < K / 32; ++b) {
+            float v[32];
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                size_t i = (size_t)r * K + (size_t)b * 32 + j;
+                v[j] = dtype == 0 ? ((const float *)x)[i] : bf16_to_f32(((const uint16_t *)x)[i]);
+                if (isnan(v[j]) || isinf(v[j]))
+                    return -1;
+                if (fabsf(v[j]) > amax)
+                    amax = fabsf(v[j]);
+            }
+            int e = 0;
+            if (amax > 0.0f) {
+                int ex;
+                frexp((double)amax, &ex);       /* amax = f * 2^ex, f in [0.5, 1) */
+#if ORACLE_MUTANT == 14
+                e = (ex - 1) - 7;               /* mutant: another element maximum exponent */
+#elif ORACLE_MUTANT == 15
+                e = ex - 8;                     /* mutant: ceiling instead of floor of log2 */
+#else
+                e = (ex - 1) - 8;
+#endif
+                if (e < -127)
+                    e = -127;
+                if (e > 127)
+                    e = 127;
+            }
+            scale_bytes[(size_t)r * (K / 32) + b] = (uint8_t)(e + 127);
+            for (int j = 0; j < 32; ++j) {
+                /* exact in fp64; representable in fp32 whenever it is not
+                   far below the smallest E4M3 step, where it rounds to zero
+                   either way */
+                float t = (float)ldexp((double)v[j], -e);
+                codes[(size_t)r * K + (size_t)b * 32 + j] = oracle_e4m3_encode(t);
+            }
+        }
+    }
+    return 0;
+}
+
+/* y[m][j] = sum over 32-wide blocks b of 2^(ea[m,b] + ew[n,b]) *
+   sum_{k in b} dec(aq[m,k]) * dec(wq[n,k]), n = cols[j] (or j), in fp64
+   (exact: every block sum is exact and the scales are powers of two);
+   bound = the same with |products|. */
+int oracle_mx_gemm(const uint8_t *aq, const uint8_t *as8, const uint8_t *wq, const uint8_t *ws8,
+                   int M, int N, int K, const int *cols, int ncols, double *y, double *bound, int nthreads)
+{
+    if (M < 0 || N < 0 || K <= 0 || K % 32 != 0 || ncols < 0)
+        return -1;
+    if (cols) {
+        for (int j = 0; j < ncols; ++j)
+            if (cols[j] < 0 || cols[j] >= N)
+                return -1;
+    } else if (ncols != N) {
+        return -1;
+    }
+    gemm_job g;
+    memset(&g, 0, sizeof g);
+    g.aq = aq; g.as8 = as8; g.wq = wq; g.ws8 = ws8;
+    g.M = M; g.N = N; g.K = K; g.cols = cols; g.ncols = ncols;
+    g.y = y; g.bound = bound;
+    oracle_e4m3_decode_table(g.table);
+    return run_columns(&g, nthreads, mx_worker);
 }

@@ -450,4 +450,75 @@ def pin_greedy_first_n_columns(o):
     assert list(tok) == [1, 0]
 
 
+# ---------------------------------------------------------------- MX (microscaling) mode
+def pin_mx_hand_values(o):
+    # amax 1.0: e = floor(log2 1) - 8 = -8 (byte 119), 1.0 -> 256 = code 0x78,
+    # 0.5 -> 128 = 0x70; amax 448: e = 0 (byte 127), 448 -> 0x7E; amax 1.9:
+    # e = -8, 1.9 * 256 = 486.4 saturates to 448 (0x7E); -0.25 * 256 = -64 =
+    # sign | exponent field 13 (2^(13-7)) = 0xE8
+    x = np.array([[1.0, 0.5] + [0.0] * 30, [448.0] + [1.0] * 31, [1.9, -0.25] + [0.1] * 30], dtype=np.float32)
+    codes, sb = o.mx_quant(x)
+    assert list(sb[:, 0]) == [119, 127, 119]
+    assert list(codes[:, 0]) == [0x78, 0x7E, 0x7E]
+    assert codes[0, 1] == 0x70 and codes[2, 1] == 0xE8 and codes[0, 2] == 0x00
+
+
+def _mx_reference(v2d):
+    """Independent restatement with numpy (exponent) and torch (E4M3 cast)."""
+    rows, K = v2d.shape
+    blocks = v2d.reshape(rows, K // 32, 32).astype(np.float64)
+    amax = np.abs(blocks).max(axis=2)
+    e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, 0).clip(-127, 127)
+    q = np.clip(blocks * np.exp2(-e)[..., None], -448.0, 448.0)
+    codes = torch.tensor(q.reshape(rows, K).astype(np.float32)).to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8).numpy(), (e + 127).astype(np.uint8)
+
+
+def pin_mx_vs_numpy_torch(o):
+    g = torch.Generator().manual_seed(61)
+    w = (torch.randn(40, 256, generator=g) * 0.02)
+    w[torch.rand(40, 256, generator=g) < 0.02] *= 30.0
+    x = torch.randn(6, 256, generator=g).to(torch.bfloat16)
+    for v, inp in ((w.numpy(), w.numpy()), (x.float().numpy(), x.view(torch.int16).numpy().view(np.uint16))):
+        codes, sb = o.mx_quant(inp)
+        rc, rs = _mx_reference(v)
+        assert np.array_equal(sb, rs)
+        assert np.array_equal(codes, rc)
+
+
+def pin_mx_pow2_equivariance(o):
+    g = torch.Generator().manual_seed(62)
+    v = (torch.randn(4, 128, generator=g)).numpy()
+    c0, s0 = o.mx_quant(v)
+    for j in (-20, -3, 5, 40):
+        c1, s1 = o.mx_quant((v * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(c1, c0) and np.array_equal(s1.astype(int), s0.astype(int) + j)
+
+
+def pin_mx_zero_block(o):
+    v = np.zeros((2, 64), dtype=np.float32)
+    v[1, :32] = -0.0
+    v[1, 32:] = 3.0
+    codes, sb = o.mx_quant(v)
+    assert list(sb.ravel()) == [127, 127, 127, 120]   # amax 3: floor(log2 3) - 8 = -7
+    assert not codes[0].any() and np.all(codes[1, :32] == 0x80)
+
+
+def pin_mx_gemm_bruteforce(o):
+    g = torch.Generator().manual_seed(63)
+    a = torch.randn(5, 192, generator=g).numpy()
+    w = (torch.randn(70, 192, generator=g) * 0.05).numpy()
+    aq, asb = o.mx_quant(a)
+    wq, wsb = o.mx_quant(w)
+    table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    A = table[aq] * np.repeat(np.exp2(asb.astype(np.float64) - 127), 32, axis=1)
+    W = table[wq] * np.repeat(np.exp2(wsb.astype(np.float64) - 127), 32, axis=1)
+    y, bound = o.mx_gemm(aq, asb, wq, wsb)
+    assert np.array_equal(y, A @ W.T) or np.allclose(y, A @ W.T, rtol=1e-15, atol=0)
+    assert np.allclose(bound, np.abs(A) @ np.abs(W).T, rtol=1e-15)
+    # a power of two on the weight scales scales Y exactly
+    y2, _ = o.mx_gemm(aq, asb, wq, (wsb.astype(int) + 3).astype(np.uint8))
+    assert np.array_equal(y2, y * 8.0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

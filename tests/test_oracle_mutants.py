@@ -22,6 +22,8 @@ MUTANTS = {
     11: "encode: overflow to NaN instead of saturating",
     12: "greedy: ties to the highest column",
     13: "greedy: -0 ranked below +0",
+    14: "MX: another element maximum exponent (7)",
+    15: "MX: ceiling instead of floor of log2(amax)",
 }
 
 
