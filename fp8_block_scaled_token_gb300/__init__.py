@@ -9,10 +9,17 @@ missing or a call fails, a RuntimeError says why.
 Entry points (same names as the C ABI):
 
 * ``fp8_quant_act(x)`` -> (xq, xs): per-token, per-128 E4M3 cast of bf16 X.
-* ``fp8_quant_weight_blocks(w)`` -> (wq, ws): 128x128-block E4M3 weights.
-* ``fp8_blockscaled_gemm(aq, as_, wq, ws)`` -> Y bf16.
+* ``fp8_quant_weight_blocks(w, tiled=False)`` -> (wq, ws): 128x128-block
+  E4M3 weights, row-major or one contiguous 16 KB run per block.
+* ``fp8_blockscaled_gemm(aq, as_, wq, ws)`` -> Y bf16 (M up to 512).
 * ``fp8_blockscaled_gemm_fused(x, wq, ws)`` -> Y bf16 (cast fused in).
-* ``bf16_gemm_ref(x, w)`` -> Y bf16 (the 16-bit output-layer baseline).
+* ``fp8_blockscaled_gemm_fused_greedy(x, wq, ws)`` -> (token, logit, Y):
+  the same plus the greedy next-token choice (M up to 64).
+* ``bf16_pack_weights_tiled(w)``, ``bf16_gemm_ref(x, w)`` -> Y bf16 (the
+  16-bit output-layer baseline).
+* ``fp8_blockscaled_gemm_workspace_size``, ``make_workspace``,
+  ``workspace_status``, ``split_plan``, ``gemm_schedule``: workspace and
+  schedule queries.
 """
 import ctypes
 import os
