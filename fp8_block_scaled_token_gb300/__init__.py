@@ -18,14 +18,16 @@ Entry points (same names as the C ABI):
 * ``bf16_pack_weights_tiled(w)``, ``bf16_gemm_ref(x, w)`` -> Y bf16 (the
   16-bit output-layer baseline).
 * ``fp8_blockscaled_gemm_workspace_size``, ``make_workspace``,
-  ``workspace_status``, ``split_plan``, ``gemm_schedule``: workspace and
-  schedule queries.
+  ``workspace_status``, ``split_plan``, ``gemm_schedule``, ``fused_route``:
+  workspace and schedule queries.
 """
+import contextlib
 import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "lib", "libfp8bs.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "lib", "libfp8bs_debug.so")
 
 FLAG_OVERLAP_PREV = 1
 FLAG_WEIGHTS_TILED = 2
@@ -40,15 +42,38 @@ class Fp8bsError(RuntimeError):
         self.code = code
 
 
+_loaded = {}
+
+
 def lib():
-    """The loaded libfp8bs.so (raises if it has not been built)."""
+    """The active copy of the library: libfp8bs.so, or libfp8bs_debug.so
+    inside ``with debug_library():``.  Raises if it has not been built."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError("libfp8bs.so is not built (expected at %s); run "
-                           "`python -c \"import __graft_entry__ as g; g.build()\"`" % LIB_PATH)
-    L = ctypes.CDLL(LIB_PATH)
+    if _lib is None:
+        _lib = _load(LIB_PATH)
+    return _lib
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Route every call of this module to libfp8bs_debug.so (the FP8BS_DEBUG
+    build, with device-side bounds checks) inside the ``with`` block."""
+    global _lib
+    prev = lib()
+    _lib = _load(DEBUG_LIB_PATH)
+    try:
+        yield _lib
+    finally:
+        _lib = prev
+
+
+def _load(path):
+    if path in _loaded:
+        return _loaded[path]
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built (expected at %s); run "
+                           "`python -c \"import __graft_entry__ as g; g.build()\"`" % (os.path.basename(path), path))
+    L = ctypes.CDLL(path)
     vp, i, u, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
     L.fp8bs_status_string.restype = ctypes.c_char_p
     L.fp8bs_status_string.argtypes = [i]
@@ -68,13 +93,21 @@ def lib():
                              ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)],
         "fp8bs_gemm_schedule": [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
                                 ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(i)],
+        "fp8bs_fused_route": [i, i, i, i, ctypes.POINTER(i)],
         "fp8bs_testhook_gemm_stall": [vp, vp, vp, vp, vp, i, i, i, vp, sz, i, ctypes.c_ulonglong, vp],
+        "fp8bs_testhook_kernel_runs": [i, i, ctypes.POINTER(ctypes.c_ulonglong)],
+        "fp8bs_testhook_gemm_fused_sms": [vp, i, vp, vp, vp, i, i, i, vp, sz, u, i, vp],
+        "fp8bs_testhook_workspace_size_sms": [i, i, i, i, ctypes.POINTER(sz)],
+        "fp8bs_testhook_debug_bad_tile": [vp, vp, vp, vp, vp, i, i, i, vp, sz, i, ctypes.c_ulonglong, vp],
+        "fp8_blockscaled_gemm_fused_noalloc": [vp, i, vp, vp, vp, i, i, i, u, vp],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
         f.restype = i
         f.argtypes = args
-    _lib = L
+    L.fp8bs_testhook_debug_build.restype = i
+    L.fp8bs_testhook_debug_build.argtypes = []
+    _loaded[path] = L
     return L
 
 
@@ -330,6 +363,15 @@ def split_plan(N, K, bf16=False, num_sms=0, cta=-1):
     _check("fp8bs_split_plan", lib().fp8bs_split_plan(N, K, 1 if bf16 else 0, num_sms, cta, ctypes.byref(c),
                                                       ctypes.byref(u), ctypes.byref(b), ctypes.byref(e)))
     return c.value, u.value, (b.value if cta >= 0 else None), (e.value if cta >= 0 else None)
+
+
+def fused_route(M, N, K, num_sms=0):
+    """'prologue' when fp8_blockscaled_gemm_fused casts the activations in the
+    GEMM kernel's prologue for this shape, 'separate' when it runs the cast as
+    its own kernel first."""
+    v = ctypes.c_int(0)
+    _check("fp8bs_fused_route", lib().fp8bs_fused_route(M, N, K, num_sms, ctypes.byref(v)))
+    return "prologue" if v.value else "separate"
 
 
 def gemm_schedule(M, N, K, num_sms=0):

@@ -1,8 +1,9 @@
 """Build libfp8bs.so in-tree for sm_103a with nvcc (no cmake, no torch
 extension machinery).  Each .cu file is one translation unit; they compile in
 parallel and link into fp8_block_scaled_token_gb300/lib/libfp8bs.so with the
-CUDA runtime linked statically.  Rebuilds only what is older than its
-sources."""
+CUDA runtime linked statically.  The same sources built with -DFP8BS_DEBUG
+(device-side bounds checks in the GEMM kernel) link into libfp8bs_debug.so.
+Rebuilds only what is older than its sources."""
 import concurrent.futures as cf
 import glob
 import os
@@ -16,6 +17,12 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfp8bs.so")
+DEBUG_LIB = os.path.join(LIBDIR, "libfp8bs_debug.so")
+# variant -> (extra nvcc flags, object directory, library)
+VARIANTS = {
+    "release": ([], OBJ, LIB),
+    "debug": (["-DFP8BS_DEBUG"], os.path.join(OBJ, "debug"), DEBUG_LIB),
+}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
@@ -43,8 +50,8 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, extra):
-    obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+def _compile(src, extra, objdir):
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     if _stale(obj, [src] + _headers()):
         cmd = [nvcc()] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -55,26 +62,38 @@ def _compile(src, extra):
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile every .cu under csrc/ and link libfp8bs.so; return its path."""
-    os.makedirs(OBJ, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
-    if force:
-        for o in glob.glob(os.path.join(OBJ, "*.o")):
-            os.remove(o)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    if _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+def _link(objs, lib):
+    if _stale(lib, objs):
+        tmp = lib + ".tmp%d" % os.getpid()
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-Xcompiler", "-fPIC", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose_ptxas: bool = False, variants=("release", "debug")) -> str:
+    """Compile every .cu under csrc/ for each variant ("release" ->
+    libfp8bs.so, "debug" -> libfp8bs_debug.so) in one parallel pool and link
+    the libraries; return the release library's path."""
+    os.makedirs(LIBDIR, exist_ok=True)
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    jobs = []
+    for v in variants:
+        flags, objdir, _ = VARIANTS[v]
+        os.makedirs(objdir, exist_ok=True)
+        if force:
+            for o in glob.glob(os.path.join(objdir, "*.o")):
+                os.remove(o)
+        extra = flags + (["-Xptxas", "-v"] if verbose_ptxas else [])
+        jobs += [(v, s, extra, objdir) for s in srcs]
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(lambda j: (j[0], _compile(j[1], j[2], j[3])), jobs))
+    for v in variants:
+        _link([o for (vv, o) in objs if vv == v], VARIANTS[v][2])
     return LIB
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                variants=("release",) if "--release-only" in sys.argv else ("release", "debug")))

@@ -15,7 +15,8 @@ namespace fp8bs {
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_dev_once[kMaxDevices];
+std::mutex g_dev_mutex;
+bool g_dev_ready[kMaxDevices];
 DeviceInfo g_dev[kMaxDevices];
 fp8bs_status g_dev_status[kMaxDevices];
 
@@ -45,21 +46,32 @@ fp8bs_status current_device(DeviceInfo *out)
         (void)cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
-    std::call_once(g_dev_once[dev], [dev]() {
-        DeviceInfo d;
-        d.device = dev;
-        fp8bs_status st = FP8BS_OK;
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-            (void)cudaGetLastError();
-            st = FP8BS_ERR_CUDA;
-        } else if (d.cc_major != 10 || d.cc_minor != 3) {
-            st = FP8BS_ERR_UNSUPPORTED_DEVICE;
+    if (!__atomic_load_n(&g_dev_ready[dev], __ATOMIC_ACQUIRE)) {
+        // First call on this device: query and cache its attributes.  A
+        // failed query is not cached, so a later call can retry.
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        if (!g_dev_ready[dev]) {
+            DeviceInfo d;
+            d.device = dev;
+            if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return FP8BS_ERR_CUDA;
+            }
+            fp8bs_status st = FP8BS_OK;
+            if (d.cc_major != 10 || d.cc_minor != 3) {
+                st = FP8BS_ERR_UNSUPPORTED_DEVICE;
+            } else {
+                d.runs = run_counters(dev);
+                if (!d.runs)
+                    return FP8BS_ERR_CUDA;
+            }
+            g_dev[dev] = d;
+            g_dev_status[dev] = st;
+            __atomic_store_n(&g_dev_ready[dev], true, __ATOMIC_RELEASE);
         }
-        g_dev[dev] = d;
-        g_dev_status[dev] = st;
-    });
+    }
     *out = g_dev[dev];
     return g_dev_status[dev];
 }
@@ -119,7 +131,8 @@ WorkspaceLayout workspace_layout(const GemmShape &sh, int M, int K)
 
 GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
 {
-    GemmShape s;
+    GemmShape s{};
+    s.m = M; // read by the fused route choice whatever the schedule below
     s.kg = mode == 2 ? K / 64 : K / 128;
     s.ntiles = (N + 127) / 128;
     s.units = static_cast<long long>(s.ntiles) * s.kg;
@@ -166,7 +179,6 @@ GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
     s.ttiles = (M + 127) / 128;
     s.units = static_cast<long long>(s.ntiles) * s.ttiles * s.kg;
     s.ctas = plan_ctas(s.units, sms);
-    s.m = M;
     return s;
 }
 
@@ -208,16 +220,19 @@ fp8bs_status quant_weight_common(const void *w, fp8bs_dtype wtype, int N, int K,
     fp8bs_status st = current_device(&dev);
     if (st != FP8BS_OK)
         return st;
-    return launch_quant_weight(w, wtype, N, K, wq, ws, tiled, static_cast<cudaStream_t>(stream));
+    return launch_quant_weight(w, wtype, N, K, wq, ws, tiled, static_cast<cudaStream_t>(stream), dev);
 }
 
-fp8bs_status gemm_workspace(int mode, int M, int N, int K, size_t *bytes)
+fp8bs_status gemm_workspace(int mode, int M, int N, int K, size_t *bytes, int sms = 0)
 {
-    DeviceInfo dev;
-    fp8bs_status st = current_device(&dev);
-    if (st != FP8BS_OK)
-        return st;
-    const GemmShape sh = gemm_shape(mode, M, N, K, dev.sms);
+    if (sms <= 0) {
+        DeviceInfo dev;
+        fp8bs_status st = current_device(&dev);
+        if (st != FP8BS_OK)
+            return st;
+        sms = dev.sms;
+    }
+    const GemmShape sh = gemm_shape(mode, M, N, K, sms);
     *bytes = workspace_layout(sh, M, K).total;
     return FP8BS_OK;
 }
@@ -228,7 +243,9 @@ fp8bs_status run_gemm(GemmLaunch &L)
     fp8bs_status st = current_device(&dev);
     if (st != FP8BS_OK)
         return st;
-    const GemmShape sh = gemm_shape(L.mode, L.M, L.N, L.K, dev.sms);
+    if (L.sms <= 0)
+        L.sms = dev.sms;
+    const GemmShape sh = gemm_shape(L.mode, L.M, L.N, L.K, L.sms);
     if (L.workspace_bytes < workspace_layout(sh, L.M, L.K).total)
         return FP8BS_ERR_WORKSPACE_TOO_SMALL;
     switch (L.mode) {
@@ -284,7 +301,7 @@ fp8bs_status fp8_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, fl
     if (st != FP8BS_OK)
         return st;
     return launch_quant_act(x, M, K, ldx, xq, xs, (flags & FP8BS_FLAG_OVERLAP_PREV) != 0,
-                            static_cast<cudaStream_t>(stream));
+                            static_cast<cudaStream_t>(stream), dev);
 }
 
 fp8bs_status fp8_quant_weight_blocks(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq, float *ws,
@@ -312,7 +329,7 @@ fp8bs_status bf16_pack_weights_tiled(const void *w, int N, int K, void *wt, void
     fp8bs_status st = current_device(&dev);
     if (st != FP8BS_OK)
         return st;
-    return launch_pack_bf16_tiled(w, N, K, wt, static_cast<cudaStream_t>(stream));
+    return launch_pack_bf16_tiled(w, N, K, wt, static_cast<cudaStream_t>(stream), dev);
 }
 
 fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, size_t *bytes)
@@ -472,7 +489,7 @@ fp8bs_status bf16_gemm_ref(const void *x, const void *w, void *y, int M, int N, 
     return run_gemm(L);
 }
 
-fp8bs_status fp8bs_workspace_status(const void *workspace, int clear, int *code)
+fp8bs_status fp8bs_workspace_status(void *workspace, int clear, int *code)
 {
     if (!workspace || !code)
         return FP8BS_ERR_INVALID_ARG;
@@ -486,7 +503,7 @@ fp8bs_status fp8bs_workspace_status(const void *workspace, int clear, int *code)
     *code = static_cast<int>(word);
     if (clear && word != 0) {
         const unsigned zero = 0;
-        if (cudaMemcpy(const_cast<void *>(workspace), &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+        if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8BS_ERR_CUDA;
         }
@@ -546,6 +563,26 @@ fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int *npad, in
     return FP8BS_OK;
 }
 
+fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, int *prologue)
+{
+    if (!prologue)
+        return FP8BS_ERR_INVALID_ARG;
+    *prologue = 0;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    int sms = num_sms;
+    if (sms <= 0) {
+        DeviceInfo dev;
+        st = current_device(&dev);
+        if (st != FP8BS_OK)
+            return st;
+        sms = dev.sms;
+    }
+    *prologue = fused_prologue_route(gemm_shape(1, M, N, K, sms)) ? 1 : 0;
+    return FP8BS_OK;
+}
+
 } // extern "C"
 
 // Test hook (declared in include/fp8bs_testing.h): the FP8 GEMM with the
@@ -585,4 +622,109 @@ extern "C" fp8bs_status fp8bs_testhook_gemm_stall(const uint8_t *aq, const float
     L.test_skip_unit = skip_unit;
     L.timeout_ns = timeout_ns;
     return run_gemm(L);
+}
+
+// Test hooks (declared in include/fp8bs_testing.h): the fused layer with its
+// schedule planned for another SM count, and the workspace that needs.
+extern "C" fp8bs_status fp8bs_testhook_workspace_size_sms(int M, int N, int K, int num_sms, size_t *bytes)
+{
+    if (!bytes || num_sms < 1 || num_sms > 4096)
+        return FP8BS_ERR_INVALID_ARG;
+    *bytes = 0;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    return gemm_workspace(1, M, N, K, bytes, num_sms);
+}
+
+extern "C" fp8bs_status fp8bs_testhook_gemm_fused_sms(const void *x, int ldx, const uint8_t *wq, const float *ws,
+                                                      void *y, int M, int N, int K, void *workspace,
+                                                      size_t workspace_bytes, unsigned flags, int num_sms,
+                                                      void *stream)
+{
+    if (!x || !wq || !ws || !y || !workspace || num_sms < 1 || num_sms > 4096)
+        return FP8BS_ERR_INVALID_ARG;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
+        return FP8BS_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||
+        !aligned(workspace, 256))
+        return FP8BS_ERR_MISALIGNED;
+    GemmLaunch L = {};
+    L.mode = 1;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.a = x;
+    L.lda = ldx;
+    L.w = wq;
+    L.ws = ws;
+    L.y = y;
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    L.flags = flags;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.test_skip_unit = -1;
+    L.timeout_ns = kDefaultTimeoutNs;
+    L.sms = num_sms;
+    return run_gemm(L);
+}
+
+// Test hook (declared in include/fp8bs_testing.h): the pre-quantised GEMM
+// with unit `bad_unit` of every CTA addressed one weight tile past the end.
+// Only the FP8BS_DEBUG build accepts it; its device-side checks must catch
+// the coordinate, skip the load and report FP8BS_ERR_DEVICE_TIMEOUT-class
+// codes in the status word (the unfilled stage's wait then runs out after
+// timeout_ns).  A coordinate past the end is safe even if a check missed
+// it: the tensor load fills such rows with zeros.
+extern "C" fp8bs_status fp8bs_testhook_debug_bad_tile(const uint8_t *aq, const float *as, const uint8_t *wq,
+                                                     const float *ws, void *y, int M, int N, int K,
+                                                     void *workspace, size_t workspace_bytes, int bad_unit,
+                                                     unsigned long long timeout_ns, void *stream)
+{
+#ifndef FP8BS_DEBUG
+    (void)aq, (void)as, (void)wq, (void)ws, (void)y, (void)M, (void)N, (void)K, (void)workspace;
+    (void)workspace_bytes, (void)bad_unit, (void)timeout_ns, (void)stream;
+    return FP8BS_ERR_INVALID_ARG; // the checks exist only in the FP8BS_DEBUG build
+#else
+    if (!aq || !as || !wq || !ws || !y || !workspace || bad_unit < 0 || timeout_ns == 0 ||
+        timeout_ns > 10ull * kDefaultTimeoutNs)
+        return FP8BS_ERR_INVALID_ARG;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    if (!aligned(aq, 16) || !aligned(wq, 16) || !aligned(as, 4) || !aligned(ws, 4) || !aligned(y, 2) ||
+        !aligned(workspace, 256))
+        return FP8BS_ERR_MISALIGNED;
+    GemmLaunch L = {};
+    L.mode = 0;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.a = aq;
+    L.lda = K;
+    L.as = as;
+    L.w = wq;
+    L.ws = ws;
+    L.y = y;
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    L.flags = 0;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.test_bad_unit = bad_unit;
+    L.timeout_ns = timeout_ns;
+    return run_gemm(L);
+#endif
+}
+
+// Whether this copy of the library was built with the device-side checks.
+extern "C" int fp8bs_testhook_debug_build(void)
+{
+#ifdef FP8BS_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }

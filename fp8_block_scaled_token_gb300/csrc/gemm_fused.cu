@@ -6,16 +6,21 @@
 
 namespace fp8bs {
 
+bool fused_prologue_route(const GemmShape &sh)
+{
+    return fused_cache_fits<kModeFp8Fused>(sh);
+}
+
 fp8bs_status launch_gemm_fused(const GemmLaunch &L, const DeviceInfo &dev)
 {
-    const GemmShape sh = gemm_shape(kModeFp8Fused, L.M, L.N, L.K, dev.sms);
-    if (fused_cache_fits<kModeFp8Fused>(sh))
+    const GemmShape sh = gemm_shape(kModeFp8Fused, L.M, L.N, L.K, L.sms > 0 ? L.sms : dev.sms);
+    if (fused_prologue_route(sh))
         return launch_gemm_mode<kModeFp8Fused>(L, dev);
     const WorkspaceLayout wl = workspace_layout(sh, L.M, L.K);
     uint8_t *aq = static_cast<uint8_t *>(L.workspace) + wl.act_off;
     float *as = reinterpret_cast<float *>(static_cast<uint8_t *>(L.workspace) + wl.act_scale_off);
     fp8bs_status st = launch_quant_act(L.a, L.M, L.K, L.lda, aq, as, (L.flags & FP8BS_FLAG_OVERLAP_PREV) != 0,
-                                       L.stream);
+                                       L.stream, dev);
     if (st != FP8BS_OK)
         return st;
     GemmLaunch G = L;

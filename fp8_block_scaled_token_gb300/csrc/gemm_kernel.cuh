@@ -47,6 +47,7 @@
 #include <cuda_bf16.h>
 #include <type_traits>
 
+#include "fp8bs_testing.h"
 #include "plan.cuh"
 #include "ptx.cuh"
 #include "quant_math.cuh"
@@ -70,6 +71,7 @@ struct GemmParams {
     int M, N, K;
     int kg;          // K blocks per tile (K/128 for FP8, K/64 for bf16)
     int ntiles;      // ceil(N / 128) weight tiles
+    int ttiles;      // token tiles
     long long units; // token tiles * ntiles * kg: unit u is K block u % kg of
                      // pair u / kg = (token tile, weight tile), weight tile fastest
     int ctas;
@@ -86,12 +88,15 @@ struct GemmParams {
     int prefetch_before_wait;// weights may be fetched before the previous grid completes
     int w_tiled;             // weights in the tiled layout (one contiguous 16 KB run per tile)
     int test_skip_unit;      // -1, or a unit whose stage the producer never fills
+    int test_bad_unit;       // -1, or a unit the producer addresses one weight tile past the end
+                             // (the FP8BS_DEBUG build's checks must catch it)
     unsigned long long timeout_ns;
     // greedy token choice (kernels instantiated with GREEDY only)
     int *token;                  // [M] chosen column per token
     float *logit;                // [M] its logit, or nullptr
     unsigned long long *best;    // workspace: [64] keys, zero between calls
     unsigned *done;              // workspace: CTAs finished, zero between calls
+    unsigned long long *runs;    // per-device launch counters (slot per instantiation)
 };
 
 // Order-preserving 32-bit key of a finite float (larger value, larger key;
@@ -201,6 +206,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     const int kb0 = static_cast<int>(u0 % kg);
 
     if (threadIdx.x == 0) {
+        if (blockIdx.x == 0)
+            atomicAdd(p.runs + FP8BS_RUNS_GEMM(MODE, NPAD, GREEDY ? 1 : 0), 1ull); // this instantiation ran
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -268,21 +275,34 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     }
                 }
             };
+            // Coordinates of one unit's loads lie inside their tensors (the
+            // FP8BS_DEBUG build checks them; weight rows past N are zero-filled).
+            auto unit_ok = [&](int stage, int k, int w, int t) {
+                return FP8BS_CHECK(stage >= 0 && stage < S && S <= C::kMaxStages && k >= 0 && k < kg && w >= 0 &&
+                                   w < p.ntiles && t >= 0 && t < p.M);
+            };
+#ifdef FP8BS_DEBUG
+            // test hook: unit test_bad_unit addresses one tile past the last
+            auto bad = [&](int i, int w) { return i == p.test_bad_unit ? p.ntiles : w; };
+#else
+            auto bad = [](int, int w) { return w; };
+#endif
             // Weights for the first ring pass, possibly before the previous grid is done.
             for (int i = 0; i < pre; ++i, step(kb, wt, trow)) {
-                if (i == p.test_skip_unit)
+                if (i == p.test_skip_unit || !unit_ok(i, kb, bad(i, wt), trow))
                     continue;
                 mbar_arrive_expect_tx(&full[i], tx);
                 armed_mask |= 1u << i;
+                const int wb = bad(i, wt);
                 const int wx = p.w_tiled ? 0 : kb * C::kChunkElems;
-                const int wy = p.w_tiled ? (wt * kg + kb) * C::kTileRows : wt * C::kTileRows;
+                const int wy = p.w_tiled ? (wb * kg + kb) * C::kTileRows : wb * C::kTileRows;
                 tma_load_2d(ring + i * C::kStageBytes, &tm_w, &full[i], wx, wy, pol_w);
             }
             grid_dependency_wait();
             if (MODE != kModeFp8Fused) {
                 int kb_b = kb0, wt_b = wt_first, trow_b = trow_first;
                 for (int i = 0; i < pre; ++i, step(kb_b, wt_b, trow_b)) {
-                    if (i == p.test_skip_unit)
+                    if (i == p.test_skip_unit || !(armed_mask & (1u << i)))
                         continue;
                     tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb_b * C::kChunkElems,
                                 trow_b, pol_b);
@@ -293,12 +313,13 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             for (int i = pre; i < nunits; ++i) {
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutProducer, p.timeout_ns))
                     break;
-                if (i != p.test_skip_unit) {
+                if (i != p.test_skip_unit && unit_ok(s, kb, bad(i, wt), trow)) {
                     mbar_arrive_expect_tx(&full[s], tx);
                     armed_mask |= 1u << s;
                     armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                    const int wb = bad(i, wt);
                     const int wx = p.w_tiled ? 0 : kb * C::kChunkElems;
-                    const int wy = p.w_tiled ? (wt * kg + kb) * C::kTileRows : wt * C::kTileRows;
+                    const int wy = p.w_tiled ? (wb * kg + kb) * C::kTileRows : wb * C::kTileRows;
                     tma_load_2d(ring + s * C::kStageBytes, &tm_w, &full[s], wx, wy, pol_w);
                     if (MODE != kModeFp8Fused)
                         tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems,
@@ -356,6 +377,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                                         p.timeout_ns))
                     break;
                 if (!mbar_wait(&full[s], ph, abort_flag, p.status, kErrTimeoutMma, p.timeout_ns))
+                    break;
+                if (MODE == kModeFp8Fused && !FP8BS_CHECK(slot < p.act_chunks))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NPAD);
@@ -427,8 +450,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     raw[b] = make_uint2(0u, 0u);
                     if (kFull || b < n) {
                         const int kbj = kb0 + cs[b] < kg ? kb0 + cs[b] : kb0 + cs[b] - kg;
-                        raw[b] = *reinterpret_cast<const uint2 *>(p.x + static_cast<long long>(ms[b]) * p.ldx +
-                                                                  kbj * 128 + lane * 4);
+                        if (FP8BS_CHECK(ms[b] >= 0 && ms[b] < p.M && kbj >= 0 && kbj < kg))
+                            raw[b] = *reinterpret_cast<const uint2 *>(p.x + static_cast<long long>(ms[b]) * p.ldx +
+                                                                      kbj * 128 + lane * 4);
                     }
                 }
                 float v[8][4], am[8];
@@ -442,7 +466,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 }
 #pragma unroll
                 for (int b = 0; b < 8; ++b) {
-                    if (kFull || b < n) {
+                    if ((kFull || b < n) && FP8BS_CHECK(cs[b] >= 0 && cs[b] < p.act_chunks && ms[b] < NPAD)) {
                         const int m = ms[b];
                         const float sc = group_scale(am[b]);
                         const uint32_t codes = quantize4(v[b][0], v[b][1], v[b][2], v[b][3], sc);
@@ -541,6 +565,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
             const int tpr = threadIdx.x - 64;
             float nx_sw = 0.0f, nx_sa = 0.0f;
             auto load_scales = [&](int wtl, int ttl, int kbb, int sl) {
+                if (!FP8BS_CHECK(wtl >= 0 && wtl < p.ntiles && kbb >= 0 && kbb < kg &&
+                                 (MODE != kModeFp8Fused || (sl >= 0 && sl < p.act_chunks))))
+                    return;
                 nx_sw = p.ws[static_cast<long long>(wtl) * kg + kbb];
                 if (MODE == kModeFp8) {
                     const int tok = ttl * NPAD + tpr;
@@ -597,15 +624,19 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     // (pre-quantised) and shuffles it to the others.
                     float sw = 1.0f, sa_l = 0.0f;
                     if constexpr (!C::kProducts && MODE != kModeBf16) {
-                        sw = p.ws[static_cast<long long>(wt) * kg + kb];
-                        if (MODE == kModeFp8 && lane < mcnt)
-                            sa_l = p.as[static_cast<long long>(tok0 + lane) * kg + kb];
+                        if (FP8BS_CHECK(wt >= 0 && wt < p.ntiles && kb >= 0 && kb < kg &&
+                                        (MODE != kModeFp8Fused || slot < p.act_chunks))) {
+                            sw = p.ws[static_cast<long long>(wt) * kg + kb];
+                            if (MODE == kModeFp8 && lane < mcnt)
+                                sa_l = p.as[static_cast<long long>(tok0 + lane) * kg + kb];
+                        }
                     }
                     const float *sa_c = act_scale + (MODE == kModeFp8Fused ? slot * NPAD : 0) + col0;
                     mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
-                    named_bar_sync(1, 32 * C::kEpiWarps);
-                    if (*abort_flag)
-                        break; // uniform across the epilogue warps
+                    // The flag may be raised by another warp at any moment; the
+                    // barrier's reduction gives every epilogue thread one answer.
+                    if (named_bar_any(1, 32 * C::kEpiWarps, *abort_flag != 0))
+                        break;
                     tc_fence_after_sync();
                     const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD + col0);
                     // 32 columns per TMEM load and wait where the tile has them
@@ -664,17 +695,20 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     const SplitPlan &pl = tile == tile_a ? plan_a : plan_b;
                     const int c_first = pl.c_first, c_last = pl.c_last;
                     auto slot_of = [&](int c) { return c == c_first ? pl.slot_first : 2 * c; };
+                    const bool ex_ok = FP8BS_CHECK(c_first >= 0 && c_first <= cta && cta <= c_last && c_last < p.ctas &&
+                                                   slot_of(cta) < 2 * p.ctas && tile >= 0 &&
+                                                   tile < p.ttiles * p.ntiles);
                     float *mine = slots_y + static_cast<long long>(slot_of(cta)) * (NPAD * 128) + col0 * 128;
 #pragma unroll
                     for (int m = 0; m < C::kCols; ++m)
-                        if (m < mcnt)
+                        if (m < mcnt && ex_ok)
                             __stcg(mine + m * 128 + row, acc[m]);
                     named_bar_sync(1, 32 * C::kEpiWarps);
                     if (warp == 2 && lane == 0) {
                         // one release for the whole epilogue group's stores (ordered
                         // by the barrier above); acquire for the others' partials
-                        const unsigned prev = atomic_add_acq_rel_gpu(&counters_y[tile], 1u);
-                        *last_flag = (prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
+                        const unsigned prev = ex_ok ? atomic_add_acq_rel_gpu(&counters_y[tile], 1u) : 0u;
+                        *last_flag = (ex_ok && prev == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
                     }
                     named_bar_sync(1, 32 * C::kEpiWarps);
                     if (*last_flag) {

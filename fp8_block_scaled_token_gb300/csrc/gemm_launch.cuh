@@ -98,6 +98,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.K = L.K;
     p.kg = sh.kg;
     p.ntiles = sh.ntiles;
+    p.ttiles = sh.ttiles;
     p.units = sh.units;
     p.ctas = sh.ctas;
     p.stages = stages;
@@ -113,11 +114,13 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.prefetch_before_wait = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
     p.w_tiled = tiled ? 1 : 0;
     p.test_skip_unit = L.test_skip_unit;
+    p.test_bad_unit = L.test_bad_unit;
     p.timeout_ns = L.timeout_ns;
     p.token = L.token;
     p.logit = L.logit;
     p.best = reinterpret_cast<unsigned long long *>(wsb + wl.greedy_off);
     p.done = reinterpret_cast<unsigned *>(wsb + wl.greedy_off + 64 * 8);
+    p.runs = dev.runs;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sh.ctas), 1, 1);
@@ -187,7 +190,7 @@ extern template fp8bs_status launch_gemm_greedy<kModeFp8Fused, true>(const GemmL
 template <int MODE>
 fp8bs_status launch_gemm_mode(const GemmLaunch &L, const DeviceInfo &dev)
 {
-    const GemmShape sh = gemm_shape(MODE, L.M, L.N, L.K, dev.sms);
+    const GemmShape sh = gemm_shape(MODE, L.M, L.N, L.K, L.sms > 0 ? L.sms : dev.sms);
     if constexpr (MODE != kModeBf16) {
         if (L.token != nullptr)
             return launch_gemm_greedy<MODE, true>(L, dev, sh);

@@ -15,6 +15,7 @@ struct DeviceInfo {
     int device = -1;
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
+    unsigned long long *runs = nullptr; // this device's kernel launch counters (runs.cu)
 };
 
 // Current device's cached attributes; status FP8BS_ERR_CUDA when there is no
@@ -69,30 +70,43 @@ struct GemmLaunch {
     size_t workspace_bytes;
     unsigned flags;
     cudaStream_t stream;
-    int test_skip_unit;       // -1 normally
+    int test_skip_unit = -1;  // -1 normally
+    int test_bad_unit = -1;   // -1 normally (FP8BS_DEBUG test hook)
     unsigned long long timeout_ns;
     int *token;               // greedy choice per token, or nullptr (then y must be set)
     float *logit;             // its logit, or nullptr
+    int sms;                  // SM count the schedule is planned for (0: the device's)
 };
 
 // Shape and SM count -> schedule; shared by launch and size queries.
 struct GemmShape {
-    int kg, ntiles, ctas, npad, m;
-    int ttiles; // token tiles (grid y)
-    bool split; // K is split across CTAs (exchange slots needed)
-    long long units;
+    int kg = 0, ntiles = 0, ctas = 0, npad = 0;
+    int m = 0;       // tokens (M)
+    int ttiles = 0;  // token tiles
+    bool split = true; // K is split across CTAs (exchange slots needed)
+    long long units = 0;
 };
 GemmShape gemm_shape(int mode, int M, int N, int K, int sms);
+
+// True when the fused entry point casts the activations in the GEMM
+// prologue for this schedule; false when it runs the separate cast kernel.
+bool fused_prologue_route(const GemmShape &sh);
+
+// Device address of the current device's kernel launch counters
+// (FP8BS_RUNS_SLOTS 64-bit words), looked up once per device; nullptr when
+// the lookup failed.
+unsigned long long *run_counters(int device);
 
 fp8bs_status launch_gemm_fp8(const GemmLaunch &L, const DeviceInfo &dev);
 fp8bs_status launch_gemm_fused(const GemmLaunch &L, const DeviceInfo &dev);
 fp8bs_status launch_gemm_bf16(const GemmLaunch &L, const DeviceInfo &dev);
 
 fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, float *xs, bool pdl,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const DeviceInfo &dev);
 fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws, bool tiled,
-                                 cudaStream_t stream);
-fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaStream_t stream);
+                                 cudaStream_t stream, const DeviceInfo &dev);
+fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaStream_t stream,
+                                    const DeviceInfo &dev);
 
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull; // one second
 

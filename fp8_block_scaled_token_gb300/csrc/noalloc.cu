@@ -12,7 +12,8 @@
 // The scratch is a file-scope __device__ array of kNoallocScratchBytes; every
 // GPU that loads the library holds it until the process exits.  Host code may
 // not use the array's name as a device address, so its address is looked up
-// once per device with cudaGetSymbolAddress and handed to the kernels.
+// once per device, with that device current, by cudaGetSymbolAddress and
+// handed to the kernels.
 #include <mutex>
 
 #include "internal.h"
@@ -25,9 +26,26 @@ constexpr size_t kNoallocScratchBytes = 12u << 20; // 12 MiB
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDev = 64;
-std::once_flag g_scratch_once[kMaxDev];
+std::mutex g_scratch_mutex;
 void *g_scratch_ptr[kMaxDev];
-cudaError_t g_scratch_err[kMaxDev];
+
+// Device address of the scratch array on `device` (the current device), or
+// an error.  A failed lookup is not remembered, so a later call retries.
+cudaError_t scratch_address(int device, void **out)
+{
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[device]) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return e;
+        if (!ptr)
+            return cudaErrorInvalidSymbol;
+        g_scratch_ptr[device] = ptr;
+    }
+    *out = g_scratch_ptr[device];
+    return cudaSuccess;
+}
 
 } // namespace
 } // namespace fp8bs
@@ -51,28 +69,25 @@ extern "C" fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ld
     fp8bs_status st = current_device(&dev);
     if (st != FP8BS_OK)
         return st;
+    if (dev.device < 0 || dev.device >= kMaxDev)
+        return FP8BS_ERR_CUDA;
     constexpr int kFused = 1; // the fused mode of the GEMM kernel
     const GemmShape sh = gemm_shape(kFused, M, N, K, dev.sms);
     const WorkspaceLayout wl = workspace_layout(sh, M, K);
     if (wl.total > kNoallocScratchBytes)
         return FP8BS_ERR_UNSUPPORTED_SHAPE; // needs more scratch than the library holds
 
-    // Once per device, with that device current: the device address of the
-    // scratch array.
-    std::call_once(g_scratch_once[dev.device], [&dev]() {
-        void *ptr = nullptr;
-        g_scratch_err[dev.device] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        g_scratch_ptr[dev.device] = ptr;
-    });
-    if (g_scratch_err[dev.device] != cudaSuccess || !g_scratch_ptr[dev.device])
-        return FP8BS_ERR_CUDA;
-    void *scratch = g_scratch_ptr[dev.device];
+    void *scratch = nullptr;
+    cudaError_t e = scratch_address(dev.device, &scratch);
+    if (e != cudaSuccess)
+        return launch_status(e);
 
     // The status word and arrival counters must start at zero; the array
     // keeps whatever the previous call left there.
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, wl.slots_off, s) != cudaSuccess)
-        return launch_status(cudaErrorUnknown);
+    e = cudaMemsetAsync(scratch, 0, wl.slots_off, s);
+    if (e != cudaSuccess)
+        return launch_status(e);
 
     GemmLaunch L = {};
     L.mode = kFused;
@@ -90,5 +105,6 @@ extern "C" fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ld
     L.stream = s;
     L.test_skip_unit = -1;
     L.timeout_ns = kDefaultTimeoutNs;
+    L.sms = dev.sms;
     return launch_gemm_fused(L, dev);
 }

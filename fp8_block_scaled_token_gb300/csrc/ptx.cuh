@@ -78,7 +78,27 @@ enum : uint32_t {
     kErrTimeoutEpilogue = 1u << 2,
     kErrTimeoutQuant = 1u << 3,
     kErrTimeoutDrain = 1u << 4,
+    kErrBounds = 1u << 5, // FP8BS_DEBUG builds: an index or coordinate left its buffer
 };
+
+// Device-side bounds checks of the FP8BS_DEBUG build (the stand-in for a
+// memory checker): a failed check records kErrBounds in the status word,
+// raises the CTA's abort flag and returns false, and the caller skips the
+// access.  Nothing traps.  In the normal build every check is the constant
+// true and compiles away.
+#ifdef FP8BS_DEBUG
+__device__ __forceinline__ bool debug_check(bool ok, unsigned *status, volatile int *abort_flag)
+{
+    if (!ok) {
+        *abort_flag = 1;
+        atomicOr(status, static_cast<unsigned>(kErrBounds));
+    }
+    return ok;
+}
+#define FP8BS_CHECK(cond) ::fp8bs::debug_check((cond), p.status, abort_flag)
+#else
+#define FP8BS_CHECK(cond) true
+#endif
 
 // Bounded wait.  Returns false when the wait gave up: either another role of
 // this CTA already raised `abort_flag`, or `timeout_ns` elapsed (then this
@@ -312,6 +332,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns, to every participating thread, whether
+// any of them passed `pred` true: one decision all of them share, even when
+// the value behind `pred` changes while they arrive.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %3, 0;\n\t"
+        "bar.red.or.pred po, %1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
 }
 
 } // namespace fp8bs

@@ -13,6 +13,7 @@
 // and the block stays in registers between the max and the conversion.
 #include <cuda_bf16.h>
 
+#include "fp8bs_testing.h"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_math.cuh"
@@ -20,8 +21,11 @@
 namespace fp8bs {
 
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
-                                                        uint8_t *__restrict__ xq, float *__restrict__ xs)
+                                                        uint8_t *__restrict__ xq, float *__restrict__ xs,
+                                                        unsigned long long *runs)
 {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        atomicAdd(runs + FP8BS_RUNS_QUANT_ACT, 1ull);
     grid_launch_dependents();
     grid_dependency_wait();
     const int kg = K / 128;
@@ -43,9 +47,12 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
 // (row r of the block at r*128), rows past N as zeros.
 template <bool kBf16, bool kTiled>
 __global__ void __launch_bounds__(256) quant_weight_kernel(const void *__restrict__ w, int N, int K,
-                                                           uint8_t *__restrict__ wq, float *__restrict__ ws)
+                                                           uint8_t *__restrict__ wq, float *__restrict__ ws,
+                                                           unsigned long long *runs)
 {
     __shared__ float warp_amax[8];
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        atomicAdd(runs + FP8BS_RUNS_QUANT_WEIGHT, 1ull);
     const int kg = K / 128;
     const long long blk = blockIdx.x;
     const int nb = static_cast<int>(blk / kg), kb = static_cast<int>(blk % kg);
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const void *__restric
 }
 
 fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, float *xs, bool pdl,
-                              cudaStream_t stream)
+                              cudaStream_t stream, const DeviceInfo &dev)
 {
     const long long groups = static_cast<long long>(M) * (K / 128);
     cudaLaunchConfig_t cfg = {};
@@ -116,14 +123,16 @@ fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq,
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return launch_status(cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const uint16_t *>(x), M, K, ldx,
-                                            xq, xs));
+                                            xq, xs, dev.runs));
 }
 
 // bf16 [N][K] -> tiled: tile (nb, kb) of 128 rows x 64 elements is one
 // contiguous 16 KB run, row r at r*128 bytes, rows past N zero.
 __global__ void __launch_bounds__(256) pack_bf16_tiled_kernel(const uint8_t *__restrict__ w, int N, int K,
-                                                              uint8_t *__restrict__ wt)
+                                                              uint8_t *__restrict__ wt, unsigned long long *runs)
 {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        atomicAdd(runs + FP8BS_RUNS_PACK_BF16, 1ull);
     const int kg = K / 64;
     const long long blk = blockIdx.x;
     const int nb = static_cast<int>(blk / kg), kb = static_cast<int>(blk % kg);
@@ -139,7 +148,8 @@ __global__ void __launch_bounds__(256) pack_bf16_tiled_kernel(const uint8_t *__r
     }
 }
 
-fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaStream_t stream)
+fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaStream_t stream,
+                                    const DeviceInfo &dev)
 {
     const long long blocks = static_cast<long long>((N + 127) / 128) * (K / 64);
     cudaLaunchConfig_t cfg = {};
@@ -147,11 +157,11 @@ fp8bs_status launch_pack_bf16_tiled(const void *w, int N, int K, void *wt, cudaS
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;
     return launch_status(cudaLaunchKernelEx(&cfg, pack_bf16_tiled_kernel, static_cast<const uint8_t *>(w), N, K,
-                                            static_cast<uint8_t *>(wt)));
+                                            static_cast<uint8_t *>(wt), dev.runs));
 }
 
 fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t *wq, float *ws, bool tiled,
-                                 cudaStream_t stream)
+                                 cudaStream_t stream, const DeviceInfo &dev)
 {
     const long long blocks = static_cast<long long>((N + 127) / 128) * (K / 128);
     cudaLaunchConfig_t cfg = {};
@@ -161,9 +171,9 @@ fp8bs_status launch_quant_weight(const void *w, int wtype, int N, int K, uint8_t
     cfg.stream = stream;
     if (wtype == FP8BS_BF16)
         return launch_status(cudaLaunchKernelEx(&cfg, tiled ? quant_weight_kernel<true, true> : quant_weight_kernel<true, false>,
-                                                w, N, K, wq, ws));
+                                                w, N, K, wq, ws, dev.runs));
     return launch_status(cudaLaunchKernelEx(&cfg, tiled ? quant_weight_kernel<false, true> : quant_weight_kernel<false, false>,
-                                            w, N, K, wq, ws));
+                                            w, N, K, wq, ws, dev.runs));
 }
 
 } // namespace fp8bs

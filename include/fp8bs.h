@@ -62,7 +62,9 @@ extern "C" {
 typedef enum fp8bs_status {
     FP8BS_OK = 0,
     FP8BS_ERR_INVALID_ARG = 1,         /* null pointer, size < 1, ldx < K, bad enum */
-    FP8BS_ERR_UNSUPPORTED_SHAPE = 2,   /* M > 64 (GEMMs), K % 128 != 0, sizes beyond 2^31 */
+    FP8BS_ERR_UNSUPPORTED_SHAPE = 2,   /* M above the entry point's limit (512 for the GEMMs, 64 with the
+                                          greedy choice or without a workspace), K not a multiple of 128
+                                          (64 for the bf16 GEMM), sizes beyond 2^30 */
     FP8BS_ERR_MISALIGNED = 3,          /* a pointer or row stride breaks the alignment stated below */
     FP8BS_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the *_workspace_size() answer */
     FP8BS_ERR_UNSUPPORTED_DEVICE = 5,  /* current device is not sm_103 */
@@ -242,6 +244,9 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx,
  * call shares the one array, so calls that can overlap on the GPU (different
  * streams without ordering) race and must not be issued.  Device-side
  * time-outs are recorded in the shared array and are not reported back.
+ * FP8BS_FLAG_OVERLAP_PREV is accepted but gives no overlap here: the kernel's
+ * programmatic dependency is on the clearing step this call enqueues, not on
+ * the caller's previous kernel.
  * Arguments and result as fp8_blockscaled_gemm_fused, with 1 <= M <= 64.
  */
 FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ldx,
@@ -280,7 +285,7 @@ FP8BS_API fp8bs_status bf16_gemm_ref(const void *x, const void *w, void *y,
  * clear != 0, resets it.  Returns FP8BS_ERR_DEVICE_TIMEOUT when the word is
  * non-zero, FP8BS_OK otherwise.
  */
-FP8BS_API fp8bs_status fp8bs_workspace_status(const void *workspace, int clear, int *code);
+FP8BS_API fp8bs_status fp8bs_workspace_status(void *workspace, int clear, int *code);
 
 /*
  * The schedule the FP8 GEMMs choose for M tokens (the plan above is its
@@ -294,6 +299,16 @@ FP8BS_API fp8bs_status fp8bs_workspace_status(const void *workspace, int clear, 
  */
 FP8BS_API fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int *npad, int *token_tiles,
                                            int *ctas, long long *units, int *split);
+
+/*
+ * The route fp8_blockscaled_gemm_fused takes for this shape: *prologue = 1
+ * when every CTA casts its own activation rows in the GEMM kernel's prologue
+ * (one kernel), 0 when the cast runs as its own kernel into the workspace
+ * before the pre-quantised GEMM (two kernels).  num_sms <= 0 means "the
+ * current device".  The choice depends only on (M, N, K, SM count).
+ * Nothing is launched.
+ */
+FP8BS_API fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, int *prologue);
 
 /*
  * The K-split schedule the GEMMs use, exposed for inspection and tests.

@@ -41,6 +41,14 @@ int main(void)
            "schedule query");
     expect(npad == 128 && tt == 4 && ctas == 152 && units == 6400 && split == 1, "schedule values at M = 512");
 
+    /* the fused entry point's route: prologue cast for the tiny workload, the
+       separate cast kernel for the square layer at 8 tokens */
+    {
+        int prologue = -1;
+        expect(fp8bs_fused_route(8, 256, 512, 152, &prologue) == FP8BS_OK && prologue == 1, "tiny: prologue");
+        expect(fp8bs_fused_route(8, 5120, 5120, 152, &prologue) == FP8BS_OK && prologue == 0, "square: separate");
+    }
+
     if (failures == 0)
         printf("ok\n");
     return failures == 0 ? 0 : 1;

@@ -35,7 +35,9 @@ def test_headers_declare_the_boundary():
     for n in ("fp8_quant_act", "fp8_quant_weight_blocks", "fp8_blockscaled_gemm",
               "fp8_blockscaled_gemm_fused", "fp8_blockscaled_gemm_workspace_size",
               "bf16_gemm_ref", "bf16_gemm_ref_workspace_size", "fp8bs_status_string",
-              "fp8bs_workspace_status", "fp8bs_split_plan"):
+              "fp8bs_workspace_status", "fp8bs_split_plan", "fp8bs_gemm_schedule", "fp8bs_fused_route",
+              "fp8_blockscaled_gemm_fused_greedy", "fp8_blockscaled_gemm_fused_noalloc",
+              "fp8bs_testhook_kernel_runs", "fp8bs_testhook_gemm_fused_sms", "fp8bs_testhook_gemm_stall"):
         assert n in names
 
 
@@ -160,6 +162,70 @@ def test_gemm_schedule_policy(L):
     assert sq(8) == dict(npad=16, token_tiles=1, ctas=152, units=1600, split=True)
     with pytest.raises(fb.Fp8bsError):
         fb.gemm_schedule(513, 5120, 5120, 152)
+
+
+def test_fused_route_policy(L):
+    """The fused entry point casts in the GEMM prologue only when every CTA
+    has at most 16 (K block, token) rows to cast; otherwise it runs the cast
+    kernel first.  The decision is a pure function of (M, N, K, SM count)."""
+    r = lambda M, N, K, sms=152: fb.fused_route(M, N, K, sms)
+    # the tiny workload: 8 units on 8 CTAs, one K block of 8 rows each
+    assert r(8, 256, 512) == "prologue"
+    # square layer: ~11 K blocks per CTA; 11 rows at M = 1, 88 at M = 8
+    assert r(1, 5120, 5120) == "prologue"
+    assert r(8, 5120, 5120) == "separate"
+    assert r(2, 2048, 1024) == "prologue" and r(16, 640, 2048) == "prologue"
+    for M, N, K in ((33, 1000, 3072), (64, 256, 512), (64, 5120, 5120), (16, 2048, 17408), (8, 248320, 5120),
+                    (65, 5120, 5120), (512, 5120, 5120)):
+        assert r(M, N, K) == "separate", (M, N, K)
+    # the rule itself, over shapes and SM counts
+    for sms in (37, 76, 148, 152):
+        for M in (1, 2, 3, 8, 16, 17, 64):
+            for N, K in ((256, 512), (640, 2048), (5120, 5120), (1000, 3072), (128, 128)):
+                s = fb.gemm_schedule(M, N, K, sms)
+                kg = K // 128
+                per_cta = -(-s["units"] // s["ctas"])
+                rows = min(per_cta, kg) * M
+                cache = min(per_cta, kg) * (s["npad"] * 128 + s["npad"] * 4)
+                want = "prologue" if rows <= 16 and cache <= 96 * 1024 else "separate"
+                assert r(M, N, K, sms) == want, (M, N, K, sms)
+    with pytest.raises(fb.Fp8bsError):
+        fb.fused_route(8, 256, 500, 152)
+
+
+def test_testing_hooks_validate_on_host(L):
+    out = (ctypes.c_ulonglong * 4)()
+    assert L.fp8bs_testhook_kernel_runs(-1, 4, out) == INVALID
+    assert L.fp8bs_testhook_kernel_runs(126, 4, out) == INVALID
+    assert L.fp8bs_testhook_kernel_runs(0, 4, None) == INVALID
+    sz = ctypes.c_size_t(7)
+    assert L.fp8bs_testhook_workspace_size_sms(8, 256, 512, 0, ctypes.byref(sz)) == INVALID
+    assert L.fp8bs_testhook_workspace_size_sms(8, 256, 500, 37, ctypes.byref(sz)) == SHAPE and sz.value == 0
+    assert L.fp8bs_testhook_workspace_size_sms(8, 5120, 5120, 37, ctypes.byref(sz)) == OK
+    assert sz.value > L_ws(8, 5120, 5120, 1) and sz.value < L_ws(8, 5120, 5120, 152)
+    f = L.fp8bs_testhook_gemm_fused_sms
+    assert f(A16, 512, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, 0, S) == INVALID       # SM count
+    assert f(A16, 512, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, 5000, S) == INVALID    # SM count
+    assert f(A1, 512, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, 37, S) == MISALIGNED
+
+
+def test_debug_library_builds_and_exports_everything(L):
+    """The FP8BS_DEBUG build links, reports itself as such, and exports the
+    same symbols; the normal build refuses the debug-only hook."""
+    fbuild.build(variants=("release", "debug"))
+    D = fb._load(fb.DEBUG_LIB_PATH)
+    assert D.fp8bs_testhook_debug_build() == 1 and L.fp8bs_testhook_debug_build() == 0
+    raw = ctypes.CDLL(fb.DEBUG_LIB_PATH)
+    for n in declared_symbols():
+        assert hasattr(raw, n), n
+    assert L.fp8bs_testhook_debug_bad_tile(A16, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, 1000, S) == INVALID
+    assert D.fp8bs_testhook_debug_bad_tile(A16, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, -1, 1000, S) == INVALID
+
+
+def L_ws(M, N, K, sms):
+    sz = ctypes.c_size_t(0)
+    assert fb.lib().fp8bs_testhook_workspace_size_sms(M, N, K, sms, ctypes.byref(sz)) == OK
+    return sz.value
 
 
 def test_c_caller_compiles_and_runs(L, tmp_path):

@@ -8,7 +8,8 @@ import torch
 import fp8_block_scaled_token_gb300 as fb
 import oracle
 from fp8_block_scaled_token_gb300 import synth
-from tests.gpu_helpers import bits16, check_y, oracle_layer
+from tests.gpu_helpers import (MODE_BF16, MODE_FP8, MODE_FUSED, RUNS_QUANT_ACT, RUNS_QUANT_WEIGHT, Ran, bits16,
+                               check_y, oracle_layer, runs_gemm)
 
 pytestmark = pytest.mark.gpu
 
@@ -83,6 +84,52 @@ def test_fused_is_bitwise_the_two_kernel_path():
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (M, N, K)
 
 
+def _tpad(M):
+    return 16 if M <= 16 else 32 if M <= 32 else 48 if M <= 48 else 64
+
+
+@pytest.mark.parametrize("M,N,K,route", [(8, 256, 512, "prologue"), (1, 5120, 5120, "prologue"),
+                                         (2, 2048, 1024, "prologue"), (16, 640, 2048, "prologue"),
+                                         (8, 5120, 5120, "separate"), (33, 1000, 3072, "separate"),
+                                         (64, 256, 512, "separate"), (16, 2048, 17408, "separate")])
+def test_fused_route_runs_the_intended_kernels(M, N, K, route):
+    """Looks inside the process: the fused entry point launches exactly the
+    kernels of the route its query names -- one prologue-cast GEMM, or the
+    cast kernel followed by the pre-quantised GEMM -- and nothing else."""
+    assert fb.fused_route(M, N, K) == route
+    x = synth.activations(M, K, seed=M + 5).cuda()
+    wq, ws = fb.fp8_quant_weight_blocks(synth.weights(N, K, seed=M + 6).cuda())
+    torch.cuda.synchronize()
+    with Ran() as r:
+        fb.fp8_blockscaled_gemm_fused(x, wq, ws)
+    if route == "prologue":
+        assert r.launched() == {runs_gemm(MODE_FUSED, _tpad(M)): 1}
+    else:
+        assert r.launched() == {RUNS_QUANT_ACT: 1, runs_gemm(MODE_FP8, _tpad(M)): 1}
+
+
+def test_entry_points_run_their_kernels():
+    M, N, K = 8, 384, 1024
+    x = synth.activations(M, K, seed=3).cuda()
+    w = synth.weights(N, K, seed=4).cuda()
+    with Ran() as r:
+        wq, ws = fb.fp8_quant_weight_blocks(w)
+    assert r.launched() == {RUNS_QUANT_WEIGHT: 1}
+    with Ran() as r:
+        xq, xs = fb.fp8_quant_act(x)
+    assert r.launched() == {RUNS_QUANT_ACT: 1}
+    with Ran() as r:
+        fb.fp8_blockscaled_gemm(xq, xs, wq, ws)
+    assert r.launched() == {runs_gemm(MODE_FP8, 16): 1}
+    with Ran() as r:
+        fb.bf16_gemm_ref(x, w.to(torch.bfloat16))
+    assert r.launched() == {runs_gemm(MODE_BF16, 16): 1}
+    with Ran() as r:
+        fb.fp8_blockscaled_gemm(fb.fp8_quant_act(synth.activations(200, K, seed=5).cuda())[0],
+                                fb.fp8_quant_act(synth.activations(200, K, seed=5).cuda())[1], wq, ws)
+    assert r.count(runs_gemm(MODE_FP8, fb.gemm_schedule(200, N, K)["npad"])) == 1
+
+
 def test_fused_row_stride():
     x_full = synth.activations(8, 1024 + 64, seed=23).cuda()
     x = x_full[:, :1024]
@@ -111,8 +158,7 @@ def test_bitwise_deterministic_over_10_runs(fused):
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
     assert fb.workspace_status(work) == 0
     # the counters are back at zero after every call
-    ctas, _, _, _ = fb.split_plan(N, K)
-    assert int(work[256:256 + 4 * ((N + 127) // 128)].view(torch.int32).abs().sum()) == 0
+    assert not work[1024:1024 + 4 * ((N + 127) // 128)].any()
 
 
 def test_overlap_flag_same_result():

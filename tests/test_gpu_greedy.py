@@ -15,7 +15,7 @@ import torch
 import fp8_block_scaled_token_gb300 as fb
 import oracle
 from fp8_block_scaled_token_gb300 import synth
-from tests.gpu_helpers import ABS_TOL, REL_TOL, bits16, oracle_layer
+from tests.gpu_helpers import ABS_TOL, MODE_FP8, MODE_FUSED, REL_TOL, RUNS_QUANT_ACT, Ran, bits16, oracle_layer, runs_gemm
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +44,14 @@ def test_greedy_matches_own_logits_and_oracle(M, N, K, tiled):
     wq, ws = fb.fp8_quant_weight_blocks(w, tiled=tiled)
     y_ref = fb.fp8_blockscaled_gemm_fused(x, wq, ws, n=N)
     work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K))
-    token, logit, y = fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, workspace=work, n=N)
-    torch.cuda.synchronize()
+    with Ran() as r:
+        token, logit, y = fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, workspace=work, n=N)
+    # the greedy instantiation of the route's GEMM is the kernel that ran
+    npad = fb.gemm_schedule(M, N, K)["npad"]
+    if fb.fused_route(M, N, K) == "prologue":
+        assert r.launched() == {runs_gemm(MODE_FUSED, npad, greedy=True): 1}
+    else:
+        assert r.launched() == {RUNS_QUANT_ACT: 1, runs_gemm(MODE_FP8, npad, greedy=True): 1}
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), "logits differ from the plain layer"
     check_against_own_logits(token, logit, y)
     check_valid_choice(token, oracle_layer(x_cpu, w_cpu))
