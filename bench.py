@@ -1,22 +1,28 @@
 """Benchmark of the small-M FP8 block-scaled linear layer on GB300.
 
-Default workload: the square decode layer, M = 8 tokens, N = K = 5120
-(E4M3 weights with 128x128 fp32 block scales, bf16 activations cast per token
-per 128 inside the GEMM, bf16 output).  One step = one batch of 8 tokens
-through one such layer: the fused activation-cast + block-scaled GEMM, one
-kernel launch.  Successive steps walk a ring of distinct weight layers whose
-total size is more than 4x the L2 cache, so every step reads its weights from
-HBM.  The timed region replays CUDA graphs of those launches (programmatic
-dependent launch lets each GEMM start streaming its weights while the previous
-one drains).
+Default workload: one decode pass at M = 8 tokens -- 256 FP8 GEMMs cycling
+the four layer shapes 5,120 x 5,120, 34,816 x 5,120, 5,120 x 17,408 and
+7,168 x 5,120 (N x K; 64 of each, every one with its own weights, 21.1 GB)
+followed by the 248,320 x 5,120 output layer (1.27 GB): 22.4 GB of E4M3
+weights with 128x128 fp32 block scales, bf16 activations cast per token per
+128 K on the way in, bf16 output.  One step = one such pass through the
+library's fused entry point (257 calls; the activation cast runs in the GEMM
+prologue or as its own kernel, whichever the library's rule picks), replayed
+from a CUDA graph with programmatic dependent launch between the layers.
+The weights (22.4 GB) are far larger than L2, so every step reads them from
+HBM.
 
-Metric: us per GEMM and achieved HBM GB/s (algorithmic bytes: Wq + s_w + X
-bf16 + Y bf16) as a fraction of the measured HBM peak.  ``value`` is the
-whole-job GB/s over all ranks.
+Metric: us per GEMM and achieved HBM GB/s (algorithmic bytes: Wq + s_w +
+X bf16 + Y bf16 per GEMM) as a fraction of the measured HBM peak.  ``value``
+is the whole-job GB/s over all ranks.  The same JSON line carries, under
+``configs``, the other workloads measured on the same weights: each layer
+shape alone (64 distinct weights cycled), the output layer at M = 1 and 8
+(FP8, with the greedy next-token choice, and the bf16 comparison GEMM), and
+the pass at M = 1 ... 512.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload square_decode|mlp_up|mlp_down|vocab|tiny] [--m M]
-                  [--configs]   (also sweep the other workloads, to stderr)
+                  [--workload decode_pass|square_decode|mlp_up|mlp_down|vocab|tiny]
+                  [--m M] [--no-sweep] [--out-dir DIR]
 
 Multi-GPU (torchrun): each rank runs its own replica on its own GPU (the
 layer needs no exchange between GPUs); the barrier + max-over-ranks timing
@@ -26,6 +32,7 @@ the parity checker) on the host cores on a bounded sample of the same
 workload.
 """
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -43,6 +50,12 @@ if ROOT not in sys.path:
 METRIC = "µs/GEMM and achieved HBM GB/s (% of GB300 peak) for FP8 block-scaled GEMM, M=1–64"
 UNIT = "GB/s"
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "quant_math.cuh", "plan.cuh", "gemm_launch.cuh"]
+
+# The decode pass: (N, K) of the four layer shapes, 64 distinct layers each in
+# this cycling order, then the output layer.
+PASS_SHAPES = ((5120, 5120), (34816, 5120), (5120, 17408), (7168, 5120))
+PASS_REPEAT = 64
+VOCAB = (248320, 5120)
 
 
 # ---------------------------------------------------------------- workloads
@@ -64,6 +77,15 @@ def algorithmic_bytes(M, N, K, fused=True):
 
 def bf16_bytes(M, N, K):
     return 2 * N * K + 2 * M * K + 2 * M * N
+
+
+def pass_layers_shapes():
+    """(N, K) of the 257 GEMMs of one decode pass, in order."""
+    return [PASS_SHAPES[i % 4] for i in range(4 * PASS_REPEAT)] + [VOCAB]
+
+
+def pass_bytes(M):
+    return sum(algorithmic_bytes(M, N, K) for N, K in pass_layers_shapes())
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -185,11 +207,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(M, N, K):
-    """DRAM bytes per launch of the GEMM from the committed ncu summary
-    (profiles/gemm_traffic.txt: "kernel_source_hash <h>" then
-    "M<m>_N<n>_K<k> <bytes per launch> ..."), if it was taken on the current
-    kernel source; else None."""
+def profiled_traffic(key):
+    """DRAM bytes (read + write) of the GEMM kernel for `key` from the
+    committed ncu summary (profiles/gemm_traffic.txt: "kernel_source_hash
+    <h>" then "<key> <bytes> ..."), if it was taken on the current kernel
+    source; else None."""
     p = os.path.join(ROOT, "profiles", "gemm_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -201,15 +223,26 @@ def profiled_traffic(M, N, K):
                 entries[parts[0]] = parts[1]
     if entries.get("kernel_source_hash") != kernel_source_hash():
         return None
-    v = entries.get("M%d_N%d_K%d" % (M, N, K))
+    v = entries.get(key)
     return None if v is None else int(v)
+
+
+def kernel_runs():
+    """The library's device-side launch counters (synchronises the device):
+    every kernel of the library adds one to its slot when it starts."""
+    import fp8_block_scaled_token_gb300 as fb
+    out = (ctypes.c_ulonglong * 128)()
+    rc = fb.lib().fp8bs_testhook_kernel_runs(0, 128, out)
+    if rc != 0:
+        raise RuntimeError("launch counters: " + fb.status_string(rc))
+    return [int(v) for v in out]
 
 
 # ---------------------------------------------------------------- CPU oracle timing
 class OracleSample:
-    """The CPU oracle on one layer: activation cast + fp64 GEMM over the first
-    `ncols` output columns, weights quantised beforehand (as on the GPU path,
-    where weight quantisation is offline)."""
+    """The CPU oracle on one layer shape: activation cast + fp64 GEMM over the
+    first `ncols` output columns, weights quantised beforehand (as on the GPU
+    path, where weight quantisation is offline)."""
 
     def __init__(self, M, N, K, seed, ncols=None):
         import numpy as np
@@ -236,381 +269,458 @@ class OracleSample:
         n, K, M = self.ncols, self.K, self.M
         return n * K + 4 * ((n + 127) // 128) * (K // 128) + 2 * M * K + 2 * M * n
 
+
+class OracleMix:
+    """The oracle on a bounded sample of a workload made of several layer
+    shapes: a slice of the output columns of every shape (an equal share of
+    the time budget each, at most 8,192 columns), run back to back.  The
+    oracle's cost per weight byte does not depend on the shape, so the
+    sampled mix gives the rate of the whole workload."""
+
+    def __init__(self, M, shapes, seconds, seed=1):
+        probe = OracleSample(M, shapes[0][0], shapes[0][1], seed, ncols=128)
+        probe.run_once()  # first run pays one-time costs
+        t0 = time.perf_counter()
+        probe.run_once()
+        per_byte = (time.perf_counter() - t0) / probe.bytes_per_run()
+        share = seconds / len(shapes)
+        self.parts = []
+        for i, (N, K) in enumerate(shapes):
+            ncols = int(max(1, min(N, 8192, share / max(per_byte * K, 1e-12))))
+            self.parts.append(OracleSample(M, N, K, seed + i, ncols=ncols))
+        self.threads = probe.threads
+        self.M = M
+        self.shapes = shapes
+
+    def run_once(self):
+        for p in self.parts:
+            p.run_once()
+
+    def bytes_per_run(self):
+        return sum(p.bytes_per_run() for p in self.parts)
+
     def describe(self):
-        return "oracle act-cast + fp64 GEMM, M=%d K=%d over %d of %d output columns, %d threads" % (
-            self.M, self.K, self.ncols, self.N, self.threads)
+        return ("oracle act-cast + fp64 GEMM at M=%d over the first %s output columns of the layer shapes %s, "
+                "%d threads" % (self.M, "/".join(str(p.ncols) for p in self.parts),
+                                ", ".join("%dx%d" % s for s in self.shapes), self.threads))
 
 
-def oracle_rate(M, N, K, seconds, seed=1):
-    """Time the oracle on the full layer for about `seconds` (at least one
-    run).  Returns (GB/s of algorithmic bytes, threads, sample text)."""
-    smp = OracleSample(M, N, K, seed)
+def oracle_rate(M, shapes, seconds, seed=1):
+    """Time the oracle on a sample of the workload for about `seconds`.
+    Returns (GB/s of algorithmic bytes, threads, sample text)."""
+    mix = OracleMix(M, shapes, seconds / 3.0, seed)
     reps, t0 = 0, time.perf_counter()
     while True:
-        smp.run_once()
+        mix.run_once()
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    gbs = smp.bytes_per_run() * reps / el / 1e9
-    return gbs, smp.threads, "%d runs of %s, %.1f s" % (reps, smp.describe(), el)
+    gbs = mix.bytes_per_run() * reps / el / 1e9
+    return gbs, mix.threads, "%d runs of %s, %.1f s" % (reps, mix.describe(), el)
+
+
+# ---------------------------------------------------------------- timing helpers
+def graph_of(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        g.replay()  # untimed: uploads the graph
+    torch.cuda.synchronize()
+    return g
+
+
+def time_replays(g, reps, stream):
+    """Seconds for `reps` replays of graph g, CUDA events on `stream`."""
+    import torch
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / 1e3
+
+
+class PassWeights:
+    """The 257 quantised weight matrices of one decode pass, resident in HBM
+    in the tiled layout (seeds 100 + i, the output layer 356)."""
+
+    def __init__(self, dev):
+        import torch
+
+        import fp8_block_scaled_token_gb300 as fb
+        from fp8_block_scaled_token_gb300 import synth
+        self.layers = []
+        for i, (N, K) in enumerate(pass_layers_shapes()):
+            w = synth.weights(N, K, seed=100 + i, device=dev)
+            self.layers.append((N, K) + fb.fp8_quant_weight_blocks(w, tiled=True))
+            del w
+        torch.cuda.synchronize()
+
+    def of_shape(self, N, K):
+        return [l for l in self.layers if l[0] == N and l[1] == K]
+
+
+class PassRunner:
+    """Buffers and the call sequence of one decode pass at M tokens."""
+
+    def __init__(self, weights, M, dev, layers=None):
+        import torch
+
+        import fp8_block_scaled_token_gb300 as fb
+        from fp8_block_scaled_token_gb300 import synth
+        self.fb = fb
+        self.layers = weights.layers if layers is None else layers
+        self.M = M
+        Ks = sorted({K for _, K, _, _ in self.layers})
+        Ns = sorted({N for N, _, _, _ in self.layers})
+        self.x = {K: synth.activations(M, K, seed=1, device=dev) for K in Ks}
+        self.y = {N: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for N in Ns}
+        wsz = max(fb.fp8_blockscaled_gemm_workspace_size(M, N, K) for N, K, _, _ in self.layers)
+        self.work = fb.make_workspace(wsz, dev)
+        self.bytes = sum(algorithmic_bytes(M, N, K) for N, K, _, _ in self.layers)
+        self.flops = sum(2.0 * M * N * K for N, K, _, _ in self.layers)
+
+    def run(self, flags=None, x=None):
+        fb = self.fb
+        f = fb.FLAG_OVERLAP_PREV if flags is None else flags
+        xs = self.x if x is None else x
+        for N, K, wq, ws in self.layers:
+            fb.fp8_blockscaled_gemm_fused(xs[K], wq, ws, y=self.y[N], workspace=self.work, flags=f, n=N)
 
 
 # ---------------------------------------------------------------- our arm
 def run_ours(args, world, rank, local):
-    import numpy as np
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if args.workload == "decode_pass":
+        run_pass(args, world, rank, dev)
+    else:
+        run_layer(args, world, rank, dev)
+
+
+def run_pass(args, world, rank, dev):
+    import torch
+
+    import fp8_block_scaled_token_gb300 as fb
+    M = args.m or 8
+    peak, peak_kind = measured_peaks()
+    weights = PassWeights(dev)
+    runner = PassRunner(weights, M, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    for _ in range(args.warmup):
+        runner.run()
+    torch.cuda.synchronize()
+    g = graph_of(runner.run, stream)
+    if fb.workspace_status(runner.work) != 0:
+        raise RuntimeError("device-side timeout during warm-up")
+
+    runs0 = kernel_runs()
+    clocks = ClockSampler(gpu_query_id(dev), args.out_dir)
+    clocks.start()
+    barrier(world)
+    elapsed = time_replays(g, args.steps, stream)
+    barrier(world)
+    clk = clocks.stop()
+    runs1 = kernel_runs()
+    launches = sum(b - a for a, b in zip(runs0, runs1))
+    t_max = max_over_ranks(elapsed, world)
+    if fb.workspace_status(runner.work) != 0:
+        raise RuntimeError("device-side timeout in the timed region")
+
+    steps = args.steps
+    value = whole_job_value(runner.bytes, steps, world, t_max)
+    per_pass_s = elapsed / steps
+    achieved = runner.bytes / per_pass_s / 1e9
+
+    # end to end through the public API, eagerly, with host buffers: the
+    # step's activations copied in from pinned host memory and the output
+    # layer's logits read back, every step
+    x_host = {K: t.cpu().pin_memory() for K, t in runner.x.items()}
+    x_dev = {K: torch.empty_like(t) for K, t in runner.x.items()}
+    yv = runner.y[VOCAB[0]]
+    y_host = torch.empty(tuple(yv.shape), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(steps, 100))
+
+    def e2e_step():
+        for K in x_dev:
+            x_dev[K].copy_(x_host[K], non_blocking=True)
+        runner.run(x=x_dev)
+        y_host.copy_(yv, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = max_over_ranks(s.elapsed_time(e) / 1e3, world)
+    e2e_value = whole_job_value(runner.bytes, e2e_steps, world, e2e_s)
+    h2d = sum(t.numel() * 2 for t in x_host.values())
+    d2h = y_host.numel() * 2
+
+    configs = []
+    if not args.no_sweep:
+        configs = sweep(weights, dev, stream, peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, threads, sample = oracle_rate(M, list(PASS_SHAPES) + [VOCAB], seconds=args.cpu_seconds)
+        cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        n_gemm = len(runner.layers)
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(t_max / steps * 1e3, 6),
+            "us_per_gemm": round(t_max / steps / n_gemm * 1e6, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe4m3->f32",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
+            "config": {"workload": "decode_pass M=%d: 256 GEMMs cycling %s (N x K, 64 distinct weights each) "
+                                   "+ the 248320x5120 output layer" % (M, ", ".join("%dx%d" % s for s in PASS_SHAPES)),
+                       "M": M, "gemms_per_step": n_gemm, "weight_bytes": sum(N * K for N, K in pass_layers_shapes()),
+                       "kernel": "fp8_blockscaled_gemm_fused (activation cast + swap-AB tcgen05 split-K GEMM)",
+                       "weights": "E4M3 tiled layout (one contiguous 16 KB run per 128x128 tile)",
+                       "l2": "inputs larger than L2: 22.4 GB of distinct weights per step",
+                       "timing": "CUDA graph of one pass replayed per step; PDL between launches; CUDA events",
+                       "parallelism": "replica per GPU" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic("pass_M%d" % M),
+                         "peak_kind": peak_kind, "kernel": "gemm_small_m_kernel (with its activation cast)",
+                         "scope": "per step: algorithmic bytes of the 257 GEMMs over the step's time",
+                         "bytes_per_step": runner.bytes, "step_us": round(per_pass_s * 1e6, 3)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "ms_per_step": round(e2e_s / e2e_steps * 1e3, 4),
+                    "how": "257 eager calls of the public fused entry point per step (no graph), activations "
+                           "copied in from pinned host memory and the output layer's logits read back"},
+            "gpu_launches": launches,
+            "gpu_launches_how": "the library's device-side launch counters, read before and after the timed region",
+            "clocks": clk,
+            "configs": configs,
+        }
+        print(json.dumps(line), flush=True)
+        if args.out_dir:
+            os.makedirs(args.out_dir, exist_ok=True)
+            with open(os.path.join(args.out_dir, "bench_line.json"), "w") as fh:
+                json.dump(line, fh, indent=1)
+
+
+def sweep(weights, dev, stream, peak):
+    """The other workloads on the pass's resident weights (printed to stderr
+    as they complete, returned for the JSON line)."""
     import torch
 
     import fp8_block_scaled_token_gb300 as fb
     from fp8_block_scaled_token_gb300 import synth
+    out = []
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    def emit(d):
+        out.append(d)
+        print(json.dumps(d), file=sys.stderr, flush=True)
+
+    def layer_row(name, M, N, K, us, nbytes):
+        return {"workload": name, "M": M, "N": N, "K": K, "us": round(us, 3), "GB/s": round(nbytes / us / 1e3, 1),
+                "frac": round(nbytes / us / 1e3 / peak, 4), "TFLOP/s": round(2.0 * M * N * K / us / 1e6, 1)}
+
+    # each layer shape alone: its 64 distinct weights cycled in one graph
+    names = {(5120, 5120): "square_decode", (34816, 5120): "mlp_up", (5120, 17408): "mlp_down",
+             (7168, 5120): "attn_7168x5120"}
+    for (N, K), name in names.items():
+        for M in ((1, 8, 64) if name == "square_decode" else (8,)):
+            r = PassRunner(weights, M, dev, layers=weights.of_shape(N, K))
+            g = graph_of(r.run, stream)
+            reps = max(1, 2000 // len(r.layers))
+            us = time_replays(g, reps, stream) * 1e6 / (reps * len(r.layers))
+            emit(layer_row(name, M, N, K, us, algorithmic_bytes(M, N, K)))
+            del g, r
+    # the output layer: FP8 plain, FP8 with the greedy choice (logits not stored)
+    vN, vK = VOCAB
+    vocab = weights.of_shape(vN, vK)
+    for M in (1, 8):
+        r = PassRunner(weights, M, dev, layers=vocab)
+        g = graph_of(r.run, stream)
+        us = time_replays(g, 50, stream) * 1e6 / 50
+        emit(layer_row("vocab", M, vN, vK, us, algorithmic_bytes(M, vN, vK)))
+        tok = torch.empty((M,), dtype=torch.int32, device=dev)
+        lg = torch.empty((M,), dtype=torch.float32, device=dev)
+        _, _, wq, ws = vocab[0]
+
+        def greedy(r=r, tok=tok, lg=lg, wq=wq, ws=ws):
+            fb.fp8_blockscaled_gemm_fused_greedy(r.x[vK], wq, ws, store_y=False, token=tok, logit=lg,
+                                                 workspace=r.work, flags=fb.FLAG_OVERLAP_PREV, n=vN)
+        g = graph_of(greedy, stream)
+        us = time_replays(g, 50, stream) * 1e6 / 50
+        emit(layer_row("vocab_greedy", M, vN, vK, us, algorithmic_bytes(M, vN, vK) - 2 * M * vN))
+        del g, r
+    # the bf16 comparison GEMM of the output layer (two distinct bf16 copies)
+    wb = [fb.bf16_pack_weights_tiled(synth.weights(vN, vK, seed=300 + i, device=dev).to(torch.bfloat16))
+          for i in range(2)]
+    for M in (1, 8):
+        x = synth.activations(M, vK, seed=4, device=dev)
+        y = torch.empty((M, vN), dtype=torch.bfloat16, device=dev)
+        work = fb.make_workspace(fb.bf16_gemm_ref_workspace_size(M, vN, vK), dev)
+
+        def f(x=x, y=y, work=work):
+            for w in wb:
+                fb.bf16_gemm_ref(x, w, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=vN)
+        g = graph_of(f, stream)
+        us = time_replays(g, 25, stream) * 1e6 / 50
+        emit(layer_row("vocab_bf16", M, vN, vK, us, bf16_bytes(M, vN, vK)))
+        del g
+    del wb
+    torch.cuda.empty_cache()
+    # the whole pass at every token count
+    for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
+        r = PassRunner(weights, M, dev)
+        g = graph_of(r.run, stream)
+        reps = 20 if M <= 64 else 5
+        s = time_replays(g, reps, stream) / reps
+        emit({"workload": "decode_pass_257", "M": M, "ms": round(s * 1e3, 4),
+              "GB/s": round(r.bytes / s / 1e9, 1), "frac": round(r.bytes / s / 1e9 / peak, 4),
+              "TFLOP/s": round(r.flops / s / 1e12, 1)})
+        del g, r
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_layer(args, world, rank, dev):
+    """One layer shape: successive steps walk a ring of distinct weight
+    layers whose total size is more than 4x the L2 cache."""
+    import torch
+
+    import fp8_block_scaled_token_gb300 as fb
+    from fp8_block_scaled_token_gb300 import synth
     cfg = workload(args.workload, args.m)
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 1024 * 1024
-    layer_bytes = N * K
-    R = max(2, min(64, math.ceil(4 * l2 / layer_bytes)))
-
-    # resident inputs: R distinct quantised layers, one activation batch
-    wqs, wss = [], []
+    R = max(2, min(64, math.ceil(4 * l2 / (N * K))))
+    layers = []
     for i in range(R):
         w = synth.weights(N, K, seed=100 + i, outlier_p=cfg.get("w_outlier_p", 0.0), device=dev)
-        wq, ws = fb.fp8_quant_weight_blocks(w, tiled=True)
-        wqs.append(wq)
-        wss.append(ws)
+        layers.append((N, K) + fb.fp8_quant_weight_blocks(w, tiled=True))
         del w
     x = synth.activations(M, K, seed=cfg["seed"], outlier_p=cfg.get("x_outlier_p", 0.0), device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K), dev)
-    flags = fb.FLAG_OVERLAP_PREV
-    torch.cuda.synchronize()
-
-    def step(i):
-        fb.fp8_blockscaled_gemm_fused(x, wqs[i % R], wss[i % R], y=y, workspace=work, flags=flags, n=N)
-
-    # warm-up (eager), then capture one ring pass and the remainder as graphs
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    steps = args.steps
-    full_reps, rem = divmod(steps, R)
     stream = torch.cuda.Stream(device=dev)
-    g_ring = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_ring, stream=stream):
-        for i in range(R):
-            step(i)
-    g_rem = None
-    if rem:
-        g_rem = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_rem, stream=stream):
-            for i in range(rem):
-                step(i)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        g_ring.replay()            # untimed: uploads the graph
-        if g_rem is not None:
-            g_rem.replay()
-    torch.cuda.synchronize()
-    if fb.workspace_status(work) != 0:
-        raise RuntimeError("device-side timeout during warm-up")
 
+    def ring():
+        for _, _, wq, ws in layers:
+            fb.fp8_blockscaled_gemm_fused(x, wq, ws, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
+
+    for _ in range(max(1, args.warmup // R + 1)):
+        ring()
+    g = graph_of(ring, stream)
+    reps = max(1, args.steps // R)
+    steps = reps * R
+    runs0 = kernel_runs()
     clocks = ClockSampler(gpu_query_id(dev), args.out_dir)
     clocks.start()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(full_reps):
-            g_ring.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
+    elapsed = time_replays(g, reps, stream)
     barrier(world)
-    elapsed = start.elapsed_time(end) / 1e3
     clk = clocks.stop()
+    launches = sum(b - a for a, b in zip(runs0, kernel_runs()))
     t_max = max_over_ranks(elapsed, world)
     if fb.workspace_status(work) != 0:
         raise RuntimeError("device-side timeout in the timed region")
-
-    bytes_step = algorithmic_bytes(M, N, K, fused=True)
-    value = whole_job_value(bytes_step, steps, world, t_max)
-    per_launch_s = elapsed / steps
-    achieved = bytes_step / per_launch_s / 1e9
+    nbytes = algorithmic_bytes(M, N, K)
     peak, peak_kind = measured_peaks()
+    achieved = nbytes / (elapsed / steps) / 1e9
 
-    # eager (no graph) for context, same launches
-    eager_steps = min(steps, 2000)
-    torch.cuda.synchronize()
-    start.record()
-    for i in range(eager_steps):
-        step(i)
-    end.record()
-    torch.cuda.synchronize()
-    eager_us = start.elapsed_time(end) * 1e3 / eager_steps
-
-    # end to end through the public API with host buffers: pinned X in, Y out, every step
     x_host = x.cpu().pin_memory()
     y_host = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
-    e2e_steps = min(steps, 5000)
-    for i in range(3):
-        x_dev.copy_(x_host, non_blocking=True)
-        fb.fp8_blockscaled_gemm_fused(x_dev, wqs[i % R], wss[i % R], y=y, workspace=work, n=N)
-        y_host.copy_(y, non_blocking=True)
-    torch.cuda.synchronize()
+    e2e_steps = min(steps, 2000)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    start.record()
+    s.record()
     for i in range(e2e_steps):
         x_dev.copy_(x_host, non_blocking=True)
-        fb.fp8_blockscaled_gemm_fused(x_dev, wqs[i % R], wss[i % R], y=y, workspace=work, n=N)
+        _, _, wq, ws = layers[i % R]
+        fb.fp8_blockscaled_gemm_fused(x_dev, wq, ws, y=y, workspace=work, n=N)
         y_host.copy_(y, non_blocking=True)
-    end.record()
+    e.record()
     torch.cuda.synchronize()
     barrier(world)
-    e2e_s = max_over_ranks(start.elapsed_time(end) / 1e3, world)
-    e2e_value = whole_job_value(bytes_step, e2e_steps, world, e2e_s)
-
-    # two-kernel path (standalone cast + GEMM) and bf16 baseline, for context
-    extra = {}
-    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    xs = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
-
-    def step2(i):
-        fb.fp8_quant_act(x, xq=xq, xs=xs, flags=flags)
-        fb.fp8_blockscaled_gemm(xq, xs, wqs[i % R], wss[i % R], y=y, workspace=work, flags=flags, n=N)
-
-    for i in range(20):
-        step2(i)
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=stream):
-        for i in range(R):
-            step2(i)
-    torch.cuda.synchronize()
-    reps2 = max(1, min(full_reps, 2000 // R + 1))
-    with torch.cuda.stream(stream):
-        g2.replay()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for _ in range(reps2):
-            g2.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    extra["two_kernel_us_per_gemm"] = start.elapsed_time(end) * 1e3 / (reps2 * R)
+    e2e_s = max_over_ranks(s.elapsed_time(e) / 1e3, world)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, threads, sample = oracle_rate(M, N, K, seconds=args.cpu_seconds, seed=cfg["seed"])
+        gbs, threads, sample = oracle_rate(M, [(N, K)], seconds=args.cpu_seconds, seed=cfg["seed"])
         cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
-
     if rank == 0:
-        traffic = profiled_traffic(M, N, K)
         line = {
-            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": steps,
-            "warmup": args.warmup, "ms_per_step": round(t_max / steps * 1e3, 6),
-            "us_per_gemm": round(t_max / steps * 1e6, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe4m3->f32",
+            "metric": METRIC, "value": round(whole_job_value(nbytes, steps, world, t_max), 3), "unit": UNIT,
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(t_max / steps * 1e3, 6),
+            "us_per_gemm": round(t_max / steps * 1e6, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3xe4m3->f32",
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
             "config": {"workload": "%s M=%d N=%d K=%d" % (args.workload, M, N, K), "M": M, "N": N, "K": K,
-                       "kernel": "fp8_blockscaled_gemm_fused (cast fused, swap-AB tcgen05, split-K)",
-                       "weights": "E4M3 tiled layout (one contiguous 16 KB run per 128x128 tile)",
-                       "weights_ring": R, "l2": "ring of %d distinct %.1f MB weight layers (%.0f MB) > 4x L2 (%.0f MB)" % (
-                           R, layer_bytes / 1e6, R * layer_bytes / 1e6, l2 / 1e6),
-                       "timing": "CUDA graphs of %d launches replayed; PDL between launches; CUDA events" % R,
+                       "weights_ring": R, "l2": "ring of %d distinct layers (%.0f MB) > 4x L2" % (R, R * N * K / 1e6),
+                       "timing": "CUDA graph of %d launches replayed; PDL between launches; CUDA events" % R,
                        "parallelism": "replica per GPU" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
-                         "peak_kind": peak_kind,
-                         "bytes_per_launch": bytes_step, "launch_us": round(per_launch_s * 1e6, 4)},
+                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic("M%d_N%d_K%d" % (M, N, K)),
+                         "peak_kind": peak_kind, "bytes_per_launch": nbytes,
+                         "launch_us": round(elapsed / steps * 1e6, 4)},
             "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": 2 * M * K,
-                    "d2h_bytes_per_step": 2 * M * N, "steps": e2e_steps,
-                    "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
-            "gpu_launches": steps,
+            "e2e": {"value": round(whole_job_value(nbytes, e2e_steps, world, e2e_s), 3), "unit": UNIT,
+                    "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N, "steps": e2e_steps},
+            "gpu_launches": launches,
             "clocks": clk,
-            "context": {"eager_us_per_gemm": round(eager_us, 3), **{k: round(v, 3) for k, v in extra.items()}},
         }
         print(json.dumps(line), flush=True)
-
-    if args.configs and rank == 0:
-        sweep(args, dev)
-
-
-# ---------------------------------------------------------------- extra configurations (stderr)
-def time_graph(fn, reps_inner, reps_outer, stream):
-    import torch
-    for i in range(3):
-        fn(i)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(reps_inner):
-            fn(i)
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        torch.cuda.synchronize()
-        s.record(stream)
-        for _ in range(reps_outer):
-            g.replay()
-        e.record(stream)
-    torch.cuda.synchronize()
-    return s.elapsed_time(e) * 1e3 / (reps_inner * reps_outer)
-
-
-PASS_SHAPES = ((5120, 5120), (34816, 5120), (5120, 17408), (7168, 5120))  # (N, K)
-
-
-def decode_pass(dev, stream, peak, Ms=(1, 2, 4, 8, 16, 32, 64, 128, 256, 512)):
-    """One decode pass: 256 GEMMs cycling the four layer shapes, every one with
-    its own weights (22.4 GB, seeds 100 + i), then the output layer; timed as
-    one graph per token count M."""
-    import torch
-
-    import fp8_block_scaled_token_gb300 as fb
-    from fp8_block_scaled_token_gb300 import synth
-    layers = []
-    for i in range(256):
-        N, K = PASS_SHAPES[i % 4]
-        w = synth.weights(N, K, seed=100 + i, device=dev)
-        layers.append((N, K) + fb.fp8_quant_weight_blocks(w, tiled=True))
-        del w
-    vN, vK = workload("vocab")["N"], workload("vocab")["K"]
-    w = synth.weights(vN, vK, seed=356, device=dev)
-    layers.append((vN, vK) + fb.fp8_quant_weight_blocks(w, tiled=True))
-    del w
-    torch.cuda.synchronize()
-    rows = []
-    for M in Ms:
-        xs = {K: synth.activations(M, K, seed=1, device=dev) for K in (5120, 17408)}
-        ys = {N: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for N, _ in PASS_SHAPES + ((vN, vK),)}
-        wsz = max(fb.fp8_blockscaled_gemm_workspace_size(M, N, K) for N, K, _, _ in layers)
-        work = fb.make_workspace(wsz, dev)
-
-        def f(i, xs=xs, ys=ys, work=work):
-            for N, K, wq, ws in layers:
-                fb.fp8_blockscaled_gemm_fused(xs[K], wq, ws, y=ys[N], workspace=work, flags=fb.FLAG_OVERLAP_PREV,
-                                              n=N)
-        us = time_graph(f, 1, 20, stream)
-        b = sum(algorithmic_bytes(M, N, K) for N, K, _, _ in layers)
-        flops = sum(2.0 * M * N * K for N, K, _, _ in layers)
-        rows.append({"workload": "decode_pass_257", "M": M, "ms": round(us / 1e3, 4),
-                     "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
-                     "TFLOP/s": round(flops / us / 1e6, 1)})
-        print(json.dumps(rows[-1]), file=sys.stderr, flush=True)
-        del xs, ys, work
-    del layers
-    torch.cuda.empty_cache()
-    return rows
-
-
-def sweep(args, dev):
-    import torch
-
-    import fp8_block_scaled_token_gb300 as fb
-    from fp8_block_scaled_token_gb300 import synth
-    peak, _ = measured_peaks()
-    stream = torch.cuda.Stream(device=dev)
-    out = []
-    l2 = 126 * 1024 * 1024
-    for name, Ms in (("square_decode", (1, 8, 64, 128, 256, 512)), ("mlp_up", (8,)), ("mlp_down", (8,)),
-                     ("vocab", (1, 8))):
-        cfg = workload(name)
-        N, K = cfg["N"], cfg["K"]
-        R = max(1, min(32, math.ceil(4 * l2 / (N * K))))
-        layers = []
-        for i in range(R):
-            w = synth.weights(N, K, seed=200 + i, outlier_p=cfg.get("w_outlier_p", 0.0), device=dev)
-            layers.append(fb.fp8_quant_weight_blocks(w, tiled=True))
-            del w
-        for M in Ms:
-            x = synth.activations(M, K, seed=cfg["seed"], outlier_p=cfg.get("x_outlier_p", 0.0), device=dev)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K), dev)
-
-            def f(i, x=x, y=y, work=work, N=N):
-                wq, ws = layers[i % R]
-                fb.fp8_blockscaled_gemm_fused(x, wq, ws, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
-            us = time_graph(f, R, max(1, 400 // R), stream)
-            b = algorithmic_bytes(M, N, K)
-            out.append({"workload": name, "M": M, "N": N, "K": K, "us": round(us, 3),
-                        "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4),
-                        "TFLOP/s": round(2.0 * M * N * K / us / 1e6, 1)})
-            print(json.dumps(out[-1]), file=sys.stderr, flush=True)
-            if name == "vocab":
-                # the output layer with the greedy token choice fused, logits not stored
-                tok = torch.empty((M,), dtype=torch.int32, device=dev)
-                lg = torch.empty((M,), dtype=torch.float32, device=dev)
-
-                def g(i, x=x, work=work, N=N, tok=tok, lg=lg):
-                    wq, ws = layers[i % R]
-                    fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, store_y=False, token=tok, logit=lg,
-                                                         workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
-                us = time_graph(g, R, max(1, 400 // R), stream)
-                b = algorithmic_bytes(M, N, K) - 2 * M * N  # no Y written
-                out.append({"workload": "vocab_greedy", "M": M, "N": N, "K": K, "us": round(us, 3),
-                            "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
-                print(json.dumps(out[-1]), file=sys.stderr, flush=True)
-        del layers
-        torch.cuda.empty_cache()
-    out += decode_pass(dev, stream, peak)
-    # vocab layer in bf16 (the 16-bit baseline of the output layer)
-    cfg = workload("vocab")
-    N, K = cfg["N"], cfg["K"]
-    wb = [fb.bf16_pack_weights_tiled(synth.weights(N, K, seed=300 + i, device=dev).to(torch.bfloat16))
-          for i in range(2)]
-    for M in (1, 8):
-        x = synth.activations(M, K, seed=4, device=dev)
-        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        work = fb.make_workspace(fb.bf16_gemm_ref_workspace_size(M, N, K), dev)
-
-        def f(i, x=x, y=y, work=work):
-            fb.bf16_gemm_ref(x, wb[i % 2], y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
-        us = time_graph(f, 2, 50, stream)
-        b = bf16_bytes(M, N, K)
-        out.append({"workload": "vocab_bf16", "M": M, "N": N, "K": K, "us": round(us, 3),
-                    "GB/s": round(b / us / 1e3, 1), "frac": round(b / us / 1e3 / peak, 4)})
-        print(json.dumps(out[-1]), file=sys.stderr, flush=True)
-    if args.out_dir:
-        os.makedirs(args.out_dir, exist_ok=True)
-        with open(os.path.join(args.out_dir, "bench_configs.json"), "w") as fh:
-            json.dump(out, fh, indent=1)
 
 
 # ---------------------------------------------------------------- reference arm: the CPU oracle
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    cfg = workload(args.workload, args.m)
-    M, N, K = cfg["M"], cfg["N"], cfg["K"]
-    # calibrate seconds per output column, then size each step so that the
-    # warm-up and timed steps together stay within about two minutes
-    probe = OracleSample(M, N, K, cfg["seed"], ncols=128)
-    t0 = time.perf_counter()
-    probe.run_once()
-    per_col = (time.perf_counter() - t0) / 128
+    if args.workload == "decode_pass":
+        M = args.m or 8
+        shapes = list(PASS_SHAPES) + [VOCAB]
+        wl = "decode_pass M=%d" % M
+    else:
+        cfg = workload(args.workload, args.m)
+        M, shapes = cfg["M"], [(cfg["N"], cfg["K"])]
+        wl = "%s M=%d N=%d K=%d" % (args.workload, M, cfg["N"], cfg["K"])
+    # size each step so that the warm-up and timed steps together stay
+    # within about two minutes
     budget = 120.0 / max(1, args.steps + args.warmup)
-    smp = OracleSample(M, N, K, cfg["seed"], ncols=int(max(1, min(N, budget / per_col))))
+    mix = OracleMix(M, shapes, budget)
     for _ in range(args.warmup):
-        smp.run_once()
+        mix.run_once()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        smp.run_once()
+        mix.run_once()
     el = time.perf_counter() - t0
-    value = smp.bytes_per_run() * args.steps / el / 1e9
-    sample = "each step: " + smp.describe()
+    value = mix.bytes_per_run() * args.steps / el / 1e9
     line = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / max(1, args.steps) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
-            "config": {"workload": "%s M=%d N=%d K=%d" % (args.workload, M, N, K), "M": M, "N": N, "K": K},
+            "config": {"workload": wl, "M": M},
             "impl": "reference",
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": smp.threads,
-                             "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": mix.threads,
+                             "sample": "each step: " + mix.describe()},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -618,16 +728,16 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="square_decode")
+    ap.add_argument("--workload", default="decode_pass")
     ap.add_argument("--m", type=int, default=None)
-    ap.add_argument("--configs", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads (configs key)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out-dir", default=None,
-                    help="directory for the clock samples and the --configs table (default: a temporary one)")
+                    help="directory for the clock samples and a copy of the JSON line (default: a temporary one)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -49,3 +49,17 @@ def test_algorithmic_bytes():
     assert bench.algorithmic_bytes(8, 248320, 5120) == 1271398400 + 310400 + 81920 + 3973120
     assert bench.bf16_bytes(8, 248320, 5120) == 2542796800 + 81920 + 3973120
     assert bench.whole_job_value(26384640, 1000, 1, 0.005) == 26384640 * 1000 / 0.005 / 1e9
+
+
+def test_decode_pass_accounting():
+    """One decode pass: 64 GEMMs of each of the four layer shapes, in cycling
+    order, then the output layer; the step's algorithmic bytes are the sum of
+    the 257 GEMMs' bytes (22.4 GB of weights)."""
+    shapes = bench.pass_layers_shapes()
+    assert len(shapes) == 257 and shapes[-1] == (248320, 5120)
+    assert shapes[:4] == [(5120, 5120), (34816, 5120), (5120, 17408), (7168, 5120)]
+    assert all(shapes.count(s) == 64 for s in bench.PASS_SHAPES)
+    weights = sum(N * K for N, K in shapes)
+    assert weights == 64 * (5120 * 5120 + 34816 * 5120 + 5120 * 17408 + 7168 * 5120) + 248320 * 5120
+    assert abs(weights / 1e9 - 22.41) < 0.01
+    assert bench.pass_bytes(8) == sum(bench.algorithmic_bytes(8, N, K) for N, K in shapes)
