@@ -17,6 +17,8 @@ Entry points (same names as the C ABI):
   the same plus the greedy next-token choice (M up to 64).
 * ``bf16_pack_weights_tiled(w)``, ``bf16_gemm_ref(x, w)`` -> Y bf16 (the
   16-bit output-layer baseline).
+* ``fp8_mx_quant_weights(w)``, ``fp8_mx_quant_act(x)``, ``fp8_mx_gemm(...)``:
+  the native block-scaled (MX) variant, one UE8M0 scale per 32 K.
 * ``fp8_blockscaled_gemm_workspace_size``, ``make_workspace``,
   ``workspace_status``, ``split_plan``, ``gemm_schedule``, ``fused_route``:
   workspace and schedule queries.
@@ -100,6 +102,10 @@ def _load(path):
         "fp8bs_testhook_workspace_size_sms": [i, i, i, i, ctypes.POINTER(sz)],
         "fp8bs_testhook_debug_bad_tile": [vp, vp, vp, vp, vp, i, i, i, vp, sz, i, ctypes.c_ulonglong, vp],
         "fp8_blockscaled_gemm_fused_noalloc": [vp, i, vp, vp, vp, i, i, i, u, vp],
+        "fp8_mx_quant_weights": [vp, i, i, i, vp, vp, vp],
+        "fp8_mx_quant_act": [vp, i, i, i, vp, vp, u, vp],
+        "fp8_mx_gemm_workspace_size": [i, i, i, ctypes.POINTER(sz)],
+        "fp8_mx_gemm": [vp, vp, vp, vp, vp, i, i, i, vp, sz, u, vp],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -342,6 +348,72 @@ def bf16_gemm_ref(x, w, y=None, workspace=None, flags=0, n=None):
     _check("bf16_gemm_ref",
            lib().bf16_gemm_ref(_ptr(x), _ptr(w), _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
                                flags, _stream()))
+    return y
+
+
+# ---------------------------------------------------------------- MX variant
+def fp8_mx_quant_weights(w, wq=None, ws_atoms=None):
+    """fp32 or bf16 W [N, K] -> (wq uint8 [ceil(N/128) * K/128, 128, 128]
+    tiled codes, ws_atoms uint8 [ceil(N/128) * K/128, 512] scale atoms):
+    one power-of-two (UE8M0) scale per 32 K per row (include/fp8bs.h)."""
+    torch = _torch()
+    if w.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("w must be float32 or bfloat16")
+    _need(w, w.dtype, "w")
+    if not w.is_contiguous():
+        raise ValueError("w must be contiguous")
+    N, K = w.shape
+    tiles = ((N + 127) // 128) * max(K // 128, 0)
+    if wq is None:
+        wq = torch.empty((tiles, 128, 128), dtype=torch.uint8, device=w.device)
+    if ws_atoms is None:
+        ws_atoms = torch.empty((tiles, 512), dtype=torch.uint8, device=w.device)
+    wt = BF16 if w.dtype == torch.bfloat16 else F32
+    _check("fp8_mx_quant_weights", lib().fp8_mx_quant_weights(_ptr(w), wt, N, K, _ptr(wq), _ptr(ws_atoms), _stream()))
+    return wq, ws_atoms
+
+
+def fp8_mx_quant_act(x, xq=None, xs_atoms=None, flags=0):
+    """bf16 X [M, K] (M <= 64; row stride may exceed K) -> (xq uint8 [M, K],
+    xs_atoms uint8 [K/128, 512])."""
+    torch = _torch()
+    _need(x, torch.bfloat16, "x")
+    _rows_contiguous(x, "x")
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if xs_atoms is None:
+        xs_atoms = torch.empty((max(K // 128, 0), 512), dtype=torch.uint8, device=x.device)
+    _check("fp8_mx_quant_act", lib().fp8_mx_quant_act(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(xs_atoms), flags,
+                                                      _stream()))
+    return xq, xs_atoms
+
+
+def fp8_mx_gemm_workspace_size(M, N, K):
+    n = ctypes.c_size_t(0)
+    _check("fp8_mx_gemm_workspace_size", lib().fp8_mx_gemm_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def fp8_mx_gemm(aq, as_atoms, wq, ws_atoms, n, y=None, workspace=None, flags=0):
+    """Y[M, n] bf16 from MX operands (fp8_mx_quant_act / fp8_mx_quant_weights;
+    n = the number of weight rows)."""
+    torch = _torch()
+    _need(aq, torch.uint8, "aq")
+    _need(as_atoms, torch.uint8, "as_atoms")
+    _need(wq, torch.uint8, "wq", ndim=3)
+    _need(ws_atoms, torch.uint8, "ws_atoms")
+    M, K = aq.shape
+    N = int(n)
+    tiles = ((N + 127) // 128) * (K // 128)
+    if wq.numel() != tiles * 16384 or ws_atoms.numel() != tiles * 512 or as_atoms.numel() != (K // 128) * 512:
+        raise ValueError("operand shapes do not agree")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)
+    if workspace is None:
+        workspace = make_workspace(fp8_mx_gemm_workspace_size(M, N, K), aq.device)
+    _check("fp8_mx_gemm", lib().fp8_mx_gemm(_ptr(aq), _ptr(as_atoms), _ptr(wq), _ptr(ws_atoms), _ptr(y), M, N, K,
+                                            _ptr(workspace), workspace.numel(), flags, _stream()))
     return y
 
 

@@ -253,6 +253,8 @@ fp8bs_status run_gemm(GemmLaunch &L)
         return launch_gemm_fp8(L, dev);
     case 1:
         return launch_gemm_fused(L, dev);
+    case 3:
+        return launch_gemm_mx(L, dev);
     default:
         return launch_gemm_bf16(L, dev);
     }
@@ -270,7 +272,8 @@ const char *fp8bs_status_string(fp8bs_status status)
     case FP8BS_ERR_INVALID_ARG:
         return "invalid argument (null pointer, size below 1, ldx below K, or unknown flag/dtype)";
     case FP8BS_ERR_UNSUPPORTED_SHAPE:
-        return "unsupported shape (GEMM M must be 1..512, 1..64 with the greedy choice; K must be a multiple of 128, or 64 for the bf16 GEMM)";
+        return "unsupported shape (GEMM M must be 1..512, 1..64 with the greedy choice, without a workspace or in "
+               "the MX variant; K must be a multiple of 128, or 64 for the bf16 GEMM)";
     case FP8BS_ERR_MISALIGNED:
         return "misaligned pointer or row stride";
     case FP8BS_ERR_WORKSPACE_TOO_SMALL:
@@ -561,6 +564,91 @@ fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int *npad, in
     *units = sh.units;
     *split = sh.split ? 1 : 0;
     return FP8BS_OK;
+}
+
+// ---------------------------------------------------------------- MX variant
+fp8bs_status fp8_mx_quant_weights(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq, uint8_t *ws_atoms,
+                                  void *stream)
+{
+    if (!w || !wq || !ws_atoms || N < 1 || K < 1 || (wtype != FP8BS_F32 && wtype != FP8BS_BF16))
+        return FP8BS_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N > (1 << 30) || K > (1 << 30) ||
+        static_cast<long long>((N + 127) / 128) * (K / 128) > 0x7FFFFFFFll)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(w, 16) || !aligned(wq, 16) || !aligned(ws_atoms, 16))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo dev;
+    fp8bs_status st = current_device(&dev);
+    if (st != FP8BS_OK)
+        return st;
+    return launch_mx_quant_weights(w, wtype, N, K, wq, ws_atoms, static_cast<cudaStream_t>(stream), dev);
+}
+
+fp8bs_status fp8_mx_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, uint8_t *xs_atoms, unsigned flags,
+                              void *stream)
+{
+    if (!x || !xq || !xs_atoms || M < 1 || K < 1 || ldx < K)
+        return FP8BS_ERR_INVALID_ARG;
+    if (check_flags(flags, FP8BS_FLAG_OVERLAP_PREV) != FP8BS_OK)
+        return FP8BS_ERR_INVALID_ARG;
+    if (M > 64 || K % 128 != 0 || K > (1 << 30))
+        return FP8BS_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(xq, 16) || !aligned(xs_atoms, 16))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo dev;
+    fp8bs_status st = current_device(&dev);
+    if (st != FP8BS_OK)
+        return st;
+    return launch_mx_quant_act(x, M, K, ldx, xq, xs_atoms, (flags & FP8BS_FLAG_OVERLAP_PREV) != 0,
+                               static_cast<cudaStream_t>(stream), dev);
+}
+
+fp8bs_status fp8_mx_gemm_workspace_size(int M, int N, int K, size_t *bytes)
+{
+    if (!bytes)
+        return FP8BS_ERR_INVALID_ARG;
+    *bytes = 0;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    if (M > 64)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE;
+    return gemm_workspace(3, M, N, K, bytes);
+}
+
+fp8bs_status fp8_mx_gemm(const uint8_t *aq, const uint8_t *as_atoms, const uint8_t *wq, const uint8_t *ws_atoms,
+                         void *y, int M, int N, int K, void *workspace, size_t workspace_bytes, unsigned flags,
+                         void *stream)
+{
+    if (!aq || !as_atoms || !wq || !ws_atoms || !y || !workspace)
+        return FP8BS_ERR_INVALID_ARG;
+    fp8bs_status st = check_gemm_shape(M, N, K, 128);
+    if (st != FP8BS_OK)
+        return st;
+    if (M > 64)
+        return FP8BS_ERR_UNSUPPORTED_SHAPE;
+    if (check_flags(flags, FP8BS_FLAG_OVERLAP_PREV) != FP8BS_OK)
+        return FP8BS_ERR_INVALID_ARG;
+    if (!aligned(aq, 16) || !aligned(as_atoms, 16) || !aligned(wq, 16) || !aligned(ws_atoms, 16) ||
+        !aligned(y, 2) || !aligned(workspace, 256))
+        return FP8BS_ERR_MISALIGNED;
+    GemmLaunch L = {};
+    L.mode = 3;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.a = aq;
+    L.lda = K;
+    L.w = wq;
+    L.sfa = ws_atoms;
+    L.sfb = as_atoms;
+    L.y = y;
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    L.flags = flags | FP8BS_FLAG_WEIGHTS_TILED; // the MX weight codes are always tiled
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.timeout_ns = kDefaultTimeoutNs;
+    return run_gemm(L);
 }
 
 fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, int *prologue)

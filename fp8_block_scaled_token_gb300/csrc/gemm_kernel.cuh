@@ -65,6 +65,7 @@ enum GemmMode : int {
     kModeFp8 = 0,      // pre-quantised activations (Aq, s_a) read by TMA
     kModeFp8Fused = 1, // bf16 activations quantised in the kernel prologue
     kModeBf16 = 2,     // bf16 x bf16, no block scales
+    kModeMx = 3,       // E4M3 x E4M3 with one UE8M0 scale per 32 K per row, applied by the tensor core
 };
 
 struct GemmParams {
@@ -79,6 +80,8 @@ struct GemmParams {
     int act_chunks;  // fused: K blocks in the activation cache (>= distinct K blocks of any CTA)
     const float *as;         // FP8: s_a [M][K/128]
     const float *ws;         // FP8: s_w [ntiles][K/128]
+    const uint8_t *sfa;      // MX: weight scale atoms [ntiles][K/128][512]
+    const uint8_t *sfb;      // MX: activation scale atoms [K/128][512]
     const uint16_t *x;       // fused: bf16 activations [M][ldx]
     int ldx;
     uint16_t *y;             // bf16 [M][N]
@@ -121,10 +124,20 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kChunkElems = MODE == kModeBf16 ? 64 : 128;
     static constexpr int kWBytes = kTileRows * kRowBytes;   // 16 KB
     static constexpr int kBBytes = NPAD * kRowBytes;        // 2..32 KB token tile
-    static constexpr int kStageBytes = kWBytes + (MODE == kModeFp8Fused ? 0 : kBBytes);
+    // MX: the stage also carries the unit's two 512-byte scale-factor atoms
+    // (weights, tokens), copied into tensor memory by the MMA thread.
+    static constexpr bool kMx = MODE == kModeMx;
+    static constexpr int kSfBytes = kMx ? 1024 : 0;
+    static constexpr int kStageBytes = kWBytes + (MODE == kModeFp8Fused ? 0 : kBBytes) + kSfBytes;
+    // bf16 and MX accumulate a whole tile segment in tensor memory (no
+    // per-K-block scale to apply on CUDA cores).
+    static constexpr bool kTileAcc = MODE == kModeBf16 || kMx;
     static constexpr int kMaxStages = 12;
     static constexpr int kAcc = NPAD == 256 ? 2 : 4;       // TMEM holds 512 fp32 columns
-    static constexpr int kTmemNeed = kAcc * NPAD;
+    // MX: after the accumulators, 8 columns of scale factors per ring stage
+    // (4 for the weight atom, 4 for the token atom).
+    static constexpr int kSfCol = kAcc * NPAD;
+    static constexpr int kTmemNeed = kAcc * NPAD + (kMx ? kMaxStages * 8 : 0);
     static constexpr int kTmemCols =
         kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
@@ -145,7 +158,7 @@ template <int NPAD, int MODE> struct GemmCfg {
     // removes a shuffle and a multiply per token per weight row.  The 16-token
     // tile (decode) keeps the per-lane scales and shuffles: there the extra
     // shared-memory round trip on the per-unit critical path cost ~0.2 us.
-    static constexpr bool kProducts = NPAD >= 32 && MODE != kModeBf16;
+    static constexpr bool kProducts = NPAD >= 32 && !kTileAcc;
     static constexpr int kProdBytes = kProducts ? 2 * NPAD * 4 : 0; // double-buffered
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     static constexpr int kHeader = 1024;                    // barriers and flags
@@ -172,6 +185,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
     using C = GemmCfg<NPAD, MODE>;
     static_assert(!GREEDY || NPAD <= 64, "the greedy choice keeps one key per token for at most 64 tokens");
     static_assert(MODE != kModeFp8Fused || NPAD <= 64, "the fused cast serves at most 64 tokens");
+    static_assert(MODE != kModeMx || (NPAD <= 64 && !GREEDY), "the MX layer serves at most 64 tokens");
     // Instantiations that only ever run one token tile (the 16-token decode
     // tile, the fused cast and the greedy choice serve at most 64 tokens):
     // pair index == weight tile, and no token-tile stepping is compiled in.
@@ -297,6 +311,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const int wx = p.w_tiled ? 0 : kb * C::kChunkElems;
                 const int wy = p.w_tiled ? (wb * kg + kb) * C::kTileRows : wb * C::kTileRows;
                 tma_load_2d(ring + i * C::kStageBytes, &tm_w, &full[i], wx, wy, pol_w);
+                if constexpr (C::kMx)
+                    bulk_load_1d(ring + i * C::kStageBytes + C::kWBytes + C::kBBytes,
+                                 p.sfa + (static_cast<long long>(wt) * kg + kb) * 512, 512, &full[i], pol_w);
             }
             grid_dependency_wait();
             if (MODE != kModeFp8Fused) {
@@ -306,6 +323,9 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         continue;
                     tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb_b * C::kChunkElems,
                                 trow_b, pol_b);
+                    if constexpr (C::kMx)
+                        bulk_load_1d(ring + i * C::kStageBytes + C::kWBytes + C::kBBytes + 512,
+                                     p.sfb + static_cast<long long>(kb_b) * 512, 512, &full[i], pol_b);
                 }
             }
             int s = pre % S;
@@ -324,6 +344,11 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     if (MODE != kModeFp8Fused)
                         tma_load_2d(ring + s * C::kStageBytes + C::kWBytes, &tm_b, &full[s], kb * C::kChunkElems,
                                     trow, pol_b);
+                    if constexpr (C::kMx) {
+                        uint8_t *sf = ring + s * C::kStageBytes + C::kWBytes + C::kBBytes;
+                        bulk_load_1d(sf, p.sfa + (static_cast<long long>(wt) * kg + kb) * 512, 512, &full[s], pol_w);
+                        bulk_load_1d(sf + 512, p.sfb + static_cast<long long>(kb) * 512, 512, &full[s], pol_b);
+                    }
                 }
                 if (++s == S) {
                     s = 0;
@@ -371,8 +396,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
                 // FP8: every K block gets a fresh accumulator (its scale differs);
                 // bf16: one accumulator per tile segment.
-                const bool fresh = (MODE != kModeBf16) || seg_start;
-                const bool publish = (MODE != kModeBf16) || seg_end;
+                const bool fresh = !C::kTileAcc || seg_start;
+                const bool publish = !C::kTileAcc || seg_end;
                 if (fresh && !mbar_wait(&tempty[acc], acc_ph ^ 1u, abort_flag, p.status, kErrTimeoutMma,
                                         p.timeout_ns))
                     break;
@@ -386,13 +411,29 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const uint8_t *b_tile = MODE == kModeFp8Fused ? act_cache + slot * C::kBBytes
                                                               : ring + s * C::kStageBytes + C::kWBytes;
                 const uint64_t b_desc = sw128_kmajor_desc(smem_u32(b_tile));
+                if constexpr (C::kMx) {
+                    // this unit's scale factors to tensor memory (per-stage
+                    // columns: the copy is ordered before the MMAs below,
+                    // and a stage's columns are rewritten only after the
+                    // MMAs that read them have completed)
+                    const uint32_t sf = tmem_base + static_cast<uint32_t>(C::kSfCol + s * 8);
+                    const uint32_t sf_smem = smem_u32(ring + s * C::kStageBytes + C::kWBytes + C::kBBytes);
+                    tmem_cp_sf_atom(sf, sf_atom_desc(sf_smem));
+                    tmem_cp_sf_atom(sf + 4, sf_atom_desc(sf_smem + 512));
 #pragma unroll
-                for (int k = 0; k < C::kMmaSteps; ++k) {
-                    const uint32_t accumulate = (k > 0 || !fresh) ? 1u : 0u;
-                    if (MODE == kModeBf16)
-                        mma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, C::kIdesc, accumulate);
-                    else
-                        mma_f8f6f4(d_tmem, a_desc + 2 * k, b_desc + 2 * k, C::kIdesc, accumulate);
+                    for (int k = 0; k < C::kMmaSteps; ++k)
+                        mma_mxf8f6f4(d_tmem, a_desc + 2 * k, b_desc + 2 * k,
+                                     idesc_mx_e4m3(C::kTileRows, NPAD, static_cast<uint32_t>(k), static_cast<uint32_t>(k)),
+                                     sf, sf + 4, (k > 0 || !fresh) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < C::kMmaSteps; ++k) {
+                        const uint32_t accumulate = (k > 0 || !fresh) ? 1u : 0u;
+                        if (MODE == kModeBf16)
+                            mma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, C::kIdesc, accumulate);
+                        else
+                            mma_f8f6f4(d_tmem, a_desc + 2 * k, b_desc + 2 * k, C::kIdesc, accumulate);
+                    }
                 }
                 mma_commit(&empty[s]);
                 if (publish) {
@@ -603,7 +644,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 const bool seg_end = (i == nunits - 1) || (kb == kg - 1);
                 if (seg_start)
                     seg_first_kb = kb;
-                if (MODE != kModeBf16 || seg_end) {
+                if (!C::kTileAcc || seg_end) {
                     // One thread per token forms s_w * s_a for this unit from
                     // the scales it loaded one unit ahead, and loads the next
                     // unit's; the barrier below publishes the products
@@ -623,7 +664,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     // 16-token tile: each lane holds the scale of token `lane`
                     // (pre-quantised) and shuffles it to the others.
                     float sw = 1.0f, sa_l = 0.0f;
-                    if constexpr (!C::kProducts && MODE != kModeBf16) {
+                    if constexpr (!C::kProducts && !C::kTileAcc) {
                         if (FP8BS_CHECK(wt >= 0 && wt < p.ntiles && kb >= 0 && kb < kg &&
                                         (MODE != kModeFp8Fused || slot < p.act_chunks))) {
                             sw = p.ws[static_cast<long long>(wt) * kg + kb];
@@ -657,7 +698,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                             for (int q = 0; q < kLd / 4; ++q)
                                 *reinterpret_cast<float4 *>(&sc[4 * q]) =
                                     reinterpret_cast<const float4 *>(pr + col0 + c * kLd)[q];
-                        } else if constexpr (MODE != kModeBf16) {
+                        } else if constexpr (!C::kTileAcc) {
 #pragma unroll
                             for (int j = 0; j < kLd; ++j)
                                 sc[j] = sw * (MODE == kModeFp8Fused ? sa_c[c * kLd + j]
@@ -667,7 +708,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                         for (int j = 0; j < kLd; ++j) {
                             const int m = c * kLd + j;
                             const float d = __uint_as_float(r[j]);
-                            if (MODE == kModeBf16)
+                            if (C::kTileAcc)
                                 acc[m] = d;
                             else
                                 acc[m] = fmaf(sc[j], d, acc[m]);

@@ -80,7 +80,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
             st = make_tmap_2d(&tm_w, L.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.N),
                               static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.K), 128, 128);
         if (st == FP8BS_OK) {
-            if (MODE == kModeFp8)
+            if (MODE == kModeFp8 || MODE == kModeMx)
                 st = make_tmap_2d(&tm_b, L.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(L.M),
                                   static_cast<uint64_t>(L.K), static_cast<uint64_t>(L.lda), 128, NPAD);
             else
@@ -105,6 +105,8 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.act_chunks = act_chunks;
     p.as = L.as;
     p.ws = L.ws;
+    p.sfa = L.sfa;
+    p.sfb = L.sfb;
     p.x = static_cast<const uint16_t *>(MODE == kModeFp8Fused ? L.a : nullptr);
     p.ldx = L.lda;
     p.y = static_cast<uint16_t *>(L.y);
@@ -163,7 +165,7 @@ fp8bs_status launch_gemm_greedy(const GemmLaunch &L, const DeviceInfo &dev, cons
 {
     // 128-token tiles exist for the plain (non-fused, non-greedy) GEMMs only;
     // the callers reject larger M before they get here.
-    if constexpr (MODE != kModeFp8Fused && !GREEDY) {
+    if constexpr (MODE != kModeFp8Fused && MODE != kModeMx && !GREEDY) {
         if (sh.npad == 128)
             return launch_gemm_npad<128, MODE, GREEDY>(L, dev, sh);
     }
@@ -191,7 +193,7 @@ template <int MODE>
 fp8bs_status launch_gemm_mode(const GemmLaunch &L, const DeviceInfo &dev)
 {
     const GemmShape sh = gemm_shape(MODE, L.M, L.N, L.K, L.sms > 0 ? L.sms : dev.sms);
-    if constexpr (MODE != kModeBf16) {
+    if constexpr (MODE == kModeFp8 || MODE == kModeFp8Fused) {
         if (L.token != nullptr)
             return launch_gemm_greedy<MODE, true>(L, dev, sh);
     }

@@ -58,13 +58,15 @@ struct GemmShape;
 WorkspaceLayout workspace_layout(const GemmShape &sh, int M, int K);
 
 struct GemmLaunch {
-    int mode;                 // GemmMode
+    int mode;                 // GemmMode (0 FP8, 1 FP8 fused cast, 2 bf16, 3 MX)
     int M, N, K;
     const void *a;            // mode 0: Aq u8 [M][K]; mode 1: X bf16 [M][ldx]; mode 2: X bf16 [M][K]
     int lda;                  // row stride of `a` in elements
     const float *as;          // mode 0
     const void *w;            // mode 0/1: Wq u8 [N][K]; mode 2: W bf16 [N][K]
     const float *ws;          // mode 0/1
+    const uint8_t *sfa;       // mode 3: weight scale atoms
+    const uint8_t *sfb;       // mode 3: activation scale atoms
     void *y;
     void *workspace;
     size_t workspace_bytes;
@@ -100,6 +102,11 @@ unsigned long long *run_counters(int device);
 fp8bs_status launch_gemm_fp8(const GemmLaunch &L, const DeviceInfo &dev);
 fp8bs_status launch_gemm_fused(const GemmLaunch &L, const DeviceInfo &dev);
 fp8bs_status launch_gemm_bf16(const GemmLaunch &L, const DeviceInfo &dev);
+fp8bs_status launch_gemm_mx(const GemmLaunch &L, const DeviceInfo &dev);
+fp8bs_status launch_mx_quant_weights(const void *w, int wtype, int N, int K, uint8_t *wq, uint8_t *sf,
+                                     cudaStream_t stream, const DeviceInfo &dev);
+fp8bs_status launch_mx_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, uint8_t *sf, bool pdl,
+                                 cudaStream_t stream, const DeviceInfo &dev);
 
 fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, float *xs, bool pdl,
                               cudaStream_t stream, const DeviceInfo &dev);

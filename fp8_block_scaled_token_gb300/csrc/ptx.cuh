@@ -156,6 +156,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory, completion counted in
+// bytes on `bar`.  Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load_1d(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                             uint64_t policy)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+                 : "memory");
+}
+
 // Fetch the 128-byte line holding `p` into this SM's L1 (no result).
 __device__ __forceinline__ void prefetch_l1(const void *p)
 {
@@ -326,6 +337,62 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ------------------------------------------ block-scaled (MX) tensor-core path
+// Scale factors of the MX MMA live in tensor memory.  They are staged in
+// shared memory as 512-byte atoms covering 128 rows (weight rows, or tokens)
+// x 4 consecutive 32-wide K blocks: the byte of row r and K block j sits at
+//     16 * (r % 32) + 4 * (r / 32) + j,
+// i.e. 32 lines of 16 bytes, line r%32 holding rows r%32, +32, +64, +96.
+// tcgen05.cp .32x128b.warpx4 copies the 32 lines into 32 lanes x 4 columns
+// of every one of the four 32-lane sub-partitions, so the sub-partition that
+// computes rows 32q..32q+31 finds row 32q + i's four bytes in its lane i,
+// column q; byte j of that column is K block j, picked per MMA by the scale
+// factor id of the instruction descriptor.
+
+// Descriptor of one such atom: no swizzle, 16-byte lines, 8-line core
+// matrices 128 bytes apart (same bit layout as sw128_kmajor_desc).
+__device__ __forceinline__ uint64_t sf_atom_desc(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 16; // leading byte offset (one core matrix wide: unused)
+    d |= static_cast<uint64_t>(128u >> 4) << 32; // stride byte offset between 8-line core matrices
+    d |= static_cast<uint64_t>(1u) << 46;        // tcgen05 descriptor version
+    return d;                                   // bits 61-63 = 0: no swizzle
+}
+
+// Copy one scale-factor atom (smem) to tensor memory columns taddr..+3 of
+// all 128 lanes (see above).  Asynchronous; ordered before later tcgen05.mma
+// of the same thread, and tracked by tcgen05.commit like them.
+__device__ __forceinline__ void tmem_cp_sf_atom(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A . sfA) * (B . sfB)^T with E4M3 operands and one UE8M0
+// scale per 32 K per row (kind::mxf8f6f4, scale vector 1X).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds:
+//   bits 4-5  scale factor id of B (byte of the 32-bit column), bits 7-9 /
+//   10-12 A / B format (0 = E4M3), bits 15/16 A/B major (0 = K-major),
+//   bits 17-22 N >> 3, bit 23 scale format (1 = UE8M0), bits 27-28 M >> 7,
+//   bits 29-30 scale factor id of A.  D is fp32.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, uint32_t a_sf_id, uint32_t b_sf_id)
+{
+    return (b_sf_id << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(m >> 7) << 27) | (a_sf_id << 29);
 }
 
 // Named barrier over `nthreads` threads (ids 1..15; 0 is __syncthreads).

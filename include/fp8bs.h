@@ -255,6 +255,52 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ldx
                                                 unsigned flags, void *stream);
 
 /*
+ * Native block-scaled (MX) variant ["Kernel-Level Optimisations for LLM
+ * Inference and Training", "Writing your own kernel": the block-scaled and
+ * MX formats that Blackwell tensor cores scale in hardware].  A different
+ * numeric contract from the 128x128 fp32 block scales above: every 32
+ * consecutive values along K of a weight row or token share one power-of-two
+ * scale 2^e, stored as the byte e + 127 (UE8M0), with
+ *   e = floor(log2(amax of the 32 values)) - 8, clamped to [-127, 127]
+ *       (0 for a block of zeros; 448 = 1.75 * 2^8 is E4M3's largest value)
+ *   code = e4m3_rn_satfinite(v / 2^e)   (exact scaling; values up to 2^9
+ *                                         saturate at 448)
+ * and Y = bf16_rn( sum over 32-blocks b of 2^(ea[m,b] + ew[n,b]) * sum_{k in b}
+ * dec(aq[m,k]) * dec(wq[n,k]) ), the scales applied by the tensor core
+ * (tcgen05.mma kind::mxf8f6f4 block_scale) with one fp32 accumulation over
+ * each CTA's share of K, so no per-block promotion runs on CUDA cores.
+ *
+ * Scale bytes are stored in 512-byte atoms, the layout the tensor core's
+ * scale-factor copy reads: per 128 rows (weight rows, or tokens) and 128 K,
+ * the byte of row r (0..127) and 32-wide K block j (0..3) is at offset
+ *   16 * (r % 32) + 4 * (r / 32) + j.
+ *
+ * fp8_mx_quant_weights: w fp32|bf16 [N][K] (16-byte aligned) ->
+ *   wq: codes in the tiled layout of fp8_quant_weight_blocks_tiled,
+ *       ceil(N/128) * 128 * K bytes, rows past N zero;
+ *   ws_atoms: ceil(N/128) * (K/128) atoms, atom (nb, kb) at
+ *       (nb * (K/128) + kb) * 512, rows past N zero.  Both 16-byte aligned.
+ * fp8_mx_quant_act: x bf16, M rows (1..64), row stride ldx (>= K, % 8 == 0),
+ *   16-byte aligned -> xq u8 [M][K] (16-byte aligned), xs_atoms: K/128
+ *   atoms, atom kb at kb * 512, token rows M..127 written as zero.  flags: 0
+ *   or FP8BS_FLAG_OVERLAP_PREV (programmatic dependent launch; x is read
+ *   after the previous kernel completes).
+ * fp8_mx_gemm: y bf16 [M][N] from those operands, 1 <= M <= 64, K % 128 == 0;
+ *   same swap-AB / TMA / split-K pipeline and the same workspace contract as
+ *   fp8_blockscaled_gemm (size from fp8_mx_gemm_workspace_size).  flags: 0
+ *   or FP8BS_FLAG_OVERLAP_PREV (the weights and their atoms may be streamed
+ *   before the previous kernel completes).  Bitwise reproducible.
+ */
+FP8BS_API fp8bs_status fp8_mx_quant_weights(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq,
+                                            uint8_t *ws_atoms, void *stream);
+FP8BS_API fp8bs_status fp8_mx_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq, uint8_t *xs_atoms,
+                                        unsigned flags, void *stream);
+FP8BS_API fp8bs_status fp8_mx_gemm_workspace_size(int M, int N, int K, size_t *bytes);
+FP8BS_API fp8bs_status fp8_mx_gemm(const uint8_t *aq, const uint8_t *as_atoms, const uint8_t *wq,
+                                   const uint8_t *ws_atoms, void *y, int M, int N, int K, void *workspace,
+                                   size_t workspace_bytes, unsigned flags, void *stream);
+
+/*
  * 16-bit comparison GEMM for the output layer [P2 "The output layer, which
  * did run": the layer "still 16-bit" before conversion]:
  *   y[m*N + n] = bf16_rn( sum_k x[m,k] * w[n,k] )   (fp32 accumulation)

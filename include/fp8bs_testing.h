@@ -25,8 +25,10 @@ extern "C" {
 #define FP8BS_RUNS_QUANT_ACT 0      /* activation quantisation kernel */
 #define FP8BS_RUNS_QUANT_WEIGHT 1   /* weight block quantisation kernel (both layouts) */
 #define FP8BS_RUNS_PACK_BF16 2      /* bf16 weight tiling kernel */
+#define FP8BS_RUNS_MX_QUANT_WEIGHT 3 /* MX weight quantisation kernel */
+#define FP8BS_RUNS_MX_QUANT_ACT 4   /* MX activation quantisation kernel */
 /* GEMM kernel instantiations: mode 0 = FP8 on pre-quantised activations,
- * 1 = FP8 with the activation cast in the kernel prologue, 2 = bf16;
+ * 1 = FP8 with the activation cast in the kernel prologue, 2 = bf16, 3 = MX;
  * npad = the token-tile width (16, 32, 48, 64, 128 or 256); greedy = 1 for
  * the instantiation with the greedy-choice epilogue. */
 #define FP8BS_RUNS_NPAD_INDEX(npad) ((npad) <= 64 ? (npad) / 16 - 1 : (npad) == 128 ? 4 : 5)

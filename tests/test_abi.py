@@ -37,7 +37,8 @@ def test_headers_declare_the_boundary():
               "bf16_gemm_ref", "bf16_gemm_ref_workspace_size", "fp8bs_status_string",
               "fp8bs_workspace_status", "fp8bs_split_plan", "fp8bs_gemm_schedule", "fp8bs_fused_route",
               "fp8_blockscaled_gemm_fused_greedy", "fp8_blockscaled_gemm_fused_noalloc",
-              "fp8bs_testhook_kernel_runs", "fp8bs_testhook_gemm_fused_sms", "fp8bs_testhook_gemm_stall"):
+              "fp8bs_testhook_kernel_runs", "fp8bs_testhook_gemm_fused_sms", "fp8bs_testhook_gemm_stall",
+              "fp8_mx_quant_weights", "fp8_mx_quant_act", "fp8_mx_gemm", "fp8_mx_gemm_workspace_size"):
         assert n in names
 
 
@@ -103,6 +104,27 @@ def test_gemm_validation(L):
     assert b(A16, A16, A16, 64, 256, 128, A16, 1 << 20, 0, S) != SHAPE
     sz = ctypes.c_size_t(5)
     assert L.fp8_blockscaled_gemm_workspace_size(8, 256, 100, ctypes.byref(sz)) == SHAPE and sz.value == 0
+
+
+def test_mx_validation(L):
+    q = L.fp8_mx_quant_weights
+    assert q(NUL, 0, 256, 512, A16, A16, S) == INVALID
+    assert q(A16, 3, 256, 512, A16, A16, S) == INVALID
+    assert q(A16, 0, 256, 160, A16, A16, S) == SHAPE                      # K % 128
+    assert q(A16, 0, 256, 512, A16, P(0x10008), S) == MISALIGNED          # atoms 16-byte aligned
+    a = L.fp8_mx_quant_act
+    assert a(A16, 65, 512, 512, A16, A16, 0, S) == SHAPE                  # at most 64 tokens
+    assert a(A16, 8, 512, 256, A16, A16, 0, S) == INVALID                 # ldx < K
+    assert a(A16, 8, 512, 512, A16, A16, 2, S) == INVALID                 # unknown flag
+    assert a(A16, 8, 512, 512, A1, A16, 0, S) == MISALIGNED
+    g = L.fp8_mx_gemm
+    assert g(A16, A16, A16, A16, A16, 65, 256, 512, A16, 1 << 20, 0, S) == SHAPE
+    assert g(A16, A16, A16, A16, A16, 8, 256, 384 + 64, A16, 1 << 20, 0, S) == SHAPE
+    assert g(A16, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 2, S) == INVALID  # tiled is implied
+    assert g(A16, P(0x10004), A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == MISALIGNED
+    assert g(NUL, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == INVALID
+    sz = ctypes.c_size_t(3)
+    assert L.fp8_mx_gemm_workspace_size(65, 256, 512, ctypes.byref(sz)) == SHAPE and sz.value == 0
 
 
 def test_split_plan_partitions_units(L):
