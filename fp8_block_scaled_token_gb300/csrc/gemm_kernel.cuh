@@ -617,6 +617,19 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     nx_sa = act_scale[sl * NPAD + tpr]; // zero for rows >= M
                 }
             };
+            // 16-token tile: the weight-block scale of the next unit and
+            // (pre-quantised activations) each lane's token scale, loaded one
+            // unit ahead so no global load sits between a finished MMA and
+            // its promotion.
+            constexpr bool kLaneScales = !C::kProducts && !C::kTileAcc;
+            float nx16_sw = 1.0f, nx16_sa = 0.0f;
+            auto load_scales16 = [&](int wtl, int kbb) {
+                if (!FP8BS_CHECK(wtl >= 0 && wtl < p.ntiles && kbb >= 0 && kbb < kg))
+                    return;
+                nx16_sw = p.ws[static_cast<long long>(wtl) * kg + kbb];
+                if (MODE == kModeFp8 && lane < mcnt)
+                    nx16_sa = p.as[static_cast<long long>(tok0 + lane) * kg + kbb];
+            };
             // Everything above is local set-up (split plans, unit state); the
             // first read of data the previous grid may write comes next, so
             // the dependency wait sits here (decode layer 11.57 -> 11.32 us).
@@ -624,6 +637,8 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                 grid_dependency_wait();
             if (C::kProducts && tpr < NPAD && nunits > 0)
                 load_scales(wt, ttile, kb, slot);
+            if (kLaneScales && nunits > 0)
+                load_scales16(wt, kb);
             for (int i = 0; i < nunits; ++i) {
                 if (i > 0) {
                     if (++kb == kg) {
@@ -664,20 +679,30 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                     // 16-token tile: each lane holds the scale of token `lane`
                     // (pre-quantised) and shuffles it to the others.
                     float sw = 1.0f, sa_l = 0.0f;
-                    if constexpr (!C::kProducts && !C::kTileAcc) {
-                        if (FP8BS_CHECK(wt >= 0 && wt < p.ntiles && kb >= 0 && kb < kg &&
-                                        (MODE != kModeFp8Fused || slot < p.act_chunks))) {
-                            sw = p.ws[static_cast<long long>(wt) * kg + kb];
-                            if (MODE == kModeFp8 && lane < mcnt)
-                                sa_l = p.as[static_cast<long long>(tok0 + lane) * kg + kb];
-                        }
+                    if constexpr (kLaneScales) {
+                        sw = nx16_sw;
+                        sa_l = nx16_sa;
+                        if (i + 1 < nunits)
+                            load_scales16(kb + 1 == kg ? wt + 1 : wt, kb + 1 == kg ? 0 : kb + 1);
                     }
-                    const float *sa_c = act_scale + (MODE == kModeFp8Fused ? slot * NPAD : 0) + col0;
+                    const bool slot_ok = MODE != kModeFp8Fused || FP8BS_CHECK(slot >= 0 && slot < p.act_chunks);
+                    const float *sa_c = act_scale + (MODE == kModeFp8Fused && slot_ok ? slot * NPAD : 0) + col0;
                     mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
-                    // The flag may be raised by another warp at any moment; the
-                    // barrier's reduction gives every epilogue thread one answer.
-                    if (named_bar_any(1, 32 * C::kEpiWarps, *abort_flag != 0))
-                        break;
+                    if constexpr (C::kProducts) {
+                        // The barrier publishes the products written above.  Its
+                        // reduction also gives every epilogue thread one answer
+                        // on the abort flag, which another warp may raise at
+                        // any moment.
+                        if (named_bar_any(1, 32 * C::kEpiWarps, *abort_flag != 0))
+                            break;
+                    }
+                    // Without a barrier here, a thread whose wait gave up
+                    // (abort) carries on through the remaining units and the
+                    // exchange with whatever the accumulator holds: every
+                    // later wait gives up after its next look at the abort
+                    // flag, every access stays in bounds, and every epilogue
+                    // warp still meets every named barrier of the exchange;
+                    // the status word reports the failure.
                     tc_fence_after_sync();
                     const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(accb * NPAD + col0);
                     // 32 columns per TMEM load and wait where the tile has them

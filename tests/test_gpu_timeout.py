@@ -51,9 +51,17 @@ def test_bounded_wait_reports_timeout_and_context_survives(M, N, K, skip):
 
 
 def test_stall_hook_rejects_bad_arguments():
-    L = fb.lib()
-    p = ctypes.c_void_p(0x10000)
-    # no skip unit, zero or too-long limit: rejected on the host
-    assert L.fp8bs_testhook_gemm_stall(p, p, p, p, p, 8, 256, 512, p, 1 << 20, -1, 1000, None) == 1
-    assert L.fp8bs_testhook_gemm_stall(p, p, p, p, p, 8, 256, 512, p, 1 << 20, 0, 0, None) == 1
-    assert L.fp8bs_testhook_gemm_stall(p, p, p, p, p, 8, 256, 512, p, 1 << 20, 0, 20_000_000_000, None) == 1
+    """No skip unit, a zero or too-long limit: rejected on the host before
+    anything is enqueued (real buffers of the stated sizes, so nothing could
+    fault even if a check were missing)."""
+    M, N, K = 8, 256, 512
+    xq = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    xs = torch.ones((M, K // 128), dtype=torch.float32, device="cuda")
+    wq = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.ones((N // 128, K // 128), dtype=torch.float32, device="cuda")
+    y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K))
+    for skip, limit in ((-1, 1000), (0, 0), (0, 20_000_000_000)):
+        assert _stall(xq, xs, wq, ws, y, M, N, K, work, skip, limit) == 1
+    torch.cuda.synchronize()
+    assert not y.any() and not work.any(), "a rejected call must not launch"
