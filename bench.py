@@ -79,6 +79,12 @@ def bf16_bytes(M, N, K):
     return 2 * N * K + 2 * M * K + 2 * M * N
 
 
+def mx_bytes(M, N, K):
+    """Bytes of one MX layer (1x32 power-of-two scales): codes + one scale
+    byte per 32 K per weight row + X bf16 + Y bf16."""
+    return N * K + N * K // 32 + 2 * M * K + 2 * M * N
+
+
 def pass_layers_shapes():
     """(N, K) of the 257 GEMMs of one decode pass, in order."""
     return [PASS_SHAPES[i % 4] for i in range(4 * PASS_REPEAT)] + [VOCAB]
@@ -584,6 +590,29 @@ def sweep(weights, dev, stream, peak):
         emit(layer_row("vocab_bf16", M, vN, vK, us, bf16_bytes(M, vN, vK)))
         del g
     del wb
+    torch.cuda.empty_cache()
+    # the native block-scaled (MX) variant: activation cast + MX GEMM per
+    # layer (a different numeric contract: 1x32 power-of-two scales), on 64
+    # distinct square layers and on the output layer
+    for (N, K), name, R in (((5120, 5120), "mx_square_decode", 64), (VOCAB, "mx_vocab", 2)):
+        mx = [fb.fp8_mx_quant_weights(synth.weights(N, K, seed=400 + i, device=dev)) for i in range(R)]
+        for M in (1, 8):
+            x = synth.activations(M, K, seed=1, device=dev)
+            xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+            xa = torch.empty((K // 128, 512), dtype=torch.uint8, device=dev)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            work = fb.make_workspace(fb.fp8_mx_gemm_workspace_size(M, N, K), dev)
+
+            def f(x=x, xq=xq, xa=xa, y=y, work=work, mx=mx, N=N):
+                for wq, wa in mx:
+                    fb.fp8_mx_quant_act(x, xq=xq, xs_atoms=xa, flags=fb.FLAG_OVERLAP_PREV)
+                    fb.fp8_mx_gemm(xq, xa, wq, wa, N, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV)
+            g = graph_of(f, stream)
+            reps = max(1, 2000 // R) if R > 2 else 25
+            us = time_replays(g, reps, stream) * 1e6 / (reps * R)
+            emit(layer_row(name, M, N, K, us, mx_bytes(M, N, K)))
+            del g
+        del mx
     torch.cuda.empty_cache()
     # the whole pass at every token count
     for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):

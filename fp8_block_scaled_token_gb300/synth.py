@@ -62,6 +62,7 @@ WORKLOADS = {
     "mlp_up": dict(M=8, N=34816, K=5120, seed=2, w_outlier_p=0.01, x_outlier_p=0.001),
     "mlp_down": dict(M=8, N=5120, K=17408, seed=3, w_outlier_p=0.01, x_outlier_p=0.001),
     "vocab": dict(M=8, N=248320, K=5120, seed=4),
+    "attn_7168": dict(M=8, N=7168, K=5120, seed=5),
 }
 
 
