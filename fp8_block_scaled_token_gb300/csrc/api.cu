@@ -158,23 +158,30 @@ GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
             return s;
         }
     }
-    // Fewer pairs than SMs: one CTA per pair over the whole K, no split and
-    // no exchange, with the widest token tile (at most 128) whose pairs still
-    // occupy at least half of the SMs; the token tiles of a weight tile read
-    // it from L2 after the first.  (256-token tiles promote 15% slower per
-    // token than 128-token ones and are not used.)
+    // Fewer pairs than SMs.  One CTA per pair over the whole K (no split, no
+    // exchange), with the widest token tile (at most 128) whose pairs fit in
+    // one wave, pays off only when those pairs leave few SMs idle for the K
+    // length: the idle fraction 1 - pairs/SMs must be at most 16/kg, i.e.
+    // pairs * (kg + 16) >= SMs * kg.  Otherwise the idle SMs' share of the
+    // bandwidth costs more than the K-split exchange.  Measured on GB300 in
+    // chains of layers (M = 128 and 256): 7,168 x 5,120 runs 112 unsplit
+    // pairs 3-5% faster than stream-K, while 5,120 x 17,408 (kg = 136) with
+    // 80 unsplit pairs is 1.5-1.7x slower than stream-K.  The token tiles of
+    // a weight tile read it from L2 after the first.  (256-token tiles
+    // promote 15% slower per token than 128-token ones and are not used.)
     for (int tt : {128, 64, 32}) {
         const int tiles_m = (M + tt - 1) / tt;
-        if (2 * static_cast<long long>(s.ntiles) * tiles_m >= sms) {
+        const long long pairs = static_cast<long long>(s.ntiles) * tiles_m;
+        if (pairs <= sms && pairs * (s.kg + 16) >= static_cast<long long>(sms) * s.kg) {
             s.npad = tt;
             s.ttiles = tiles_m;
-            s.units = static_cast<long long>(s.ntiles) * tiles_m * s.kg;
-            s.ctas = s.ntiles * tiles_m; // one pair per CTA
+            s.units = pairs * s.kg;
+            s.ctas = static_cast<int>(pairs); // one pair per CTA
             s.split = false;
             return s;
         }
     }
-    // Too few weight tiles for that: stream-K over 128-token pairs.
+    // Otherwise: stream-K over 128-token pairs.
     s.npad = 128;
     s.ttiles = (M + 127) / 128;
     s.units = static_cast<long long>(s.ntiles) * s.ttiles * s.kg;

@@ -145,12 +145,17 @@ template <int NPAD, int MODE> struct GemmCfg {
     // ring each): the next GEMM's CTA, launched early by programmatic
     // dependent launch, then shares the SM and streams its weights while this
     // one finishes.  Measured on GB300 this beats one CTA per SM with a
-    // 200 KB ring for every layer shape of the workloads at M <= 16, and
-    // loses at M = 32 (and the wider accumulators of NPAD >= 48 would spill).
+    // 200 KB ring for every layer shape of the workloads at M <= 16.  At
+    // M = 32 and 48 it loses by 5% and 11% over a whole decode pass (cast
+    // kernels included), although it wins by 2-5% in a chain of
+    // pre-quantised layers.
     static constexpr int kMinBlocks = (MODE != kModeFp8Fused && NPAD == 16) ? 2 : 1;
-    // A 256-token tile splits its columns over two groups of four epilogue
-    // warps, so a thread keeps at most 128 accumulators in registers.
-    static constexpr int kColGroups = NPAD > 128 ? 2 : 1;
+    // From 64 tokens up the columns of a token tile are split over two groups
+    // of four epilogue warps: twice the threads promote each unit, which the
+    // wider tiles need more than a second resident CTA (measured in a chain
+    // of layers: 64-token tiles 7-16% faster than with one group, 128-token
+    // tiles 1-13%), and a thread keeps at most 128 accumulators in registers.
+    static constexpr int kColGroups = NPAD >= 64 ? 2 : 1;
     static constexpr int kCols = NPAD / kColGroups;         // token columns per epilogue thread
     static constexpr int kEpiWarps = 4 * kColGroups;
     // From 32 tokens up, the per-unit scale products s_w * s_a[m] are formed
@@ -161,6 +166,19 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr bool kProducts = NPAD >= 32 && !kTileAcc;
     static constexpr int kProdBytes = kProducts ? 2 * NPAD * 4 : 0; // double-buffered
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
+    // Registers per thread.  An SM's register file is four 16,384-register
+    // banks, one per scheduler, and a CTA's warps are spread over the four:
+    // with W resident warps a bank holds ceil(W / 4) of them, so a thread may
+    // have at most 16,384 / (32 * ceil(W / 4)) (rounded down to 8, at most
+    // 255).  With two CTAs per SM the cap is lower, 160: next to two GEMM
+    // CTAs (three 5,120-register warps per bank) the activation cast's
+    // 4-warp CTA (one 1,024-register warp per bank at 32 registers) still
+    // fits, so the next GEMM's early CTA is not kept off an SM where a cast
+    // CTA landed (decode pass 5.31 -> 5.27 ms at M = 8).
+    static constexpr int kWarpsPerBank = (kMinBlocks * (kThreads / 32) + 3) / 4;
+    static constexpr int kRegSplit = (16384 / (32 * kWarpsPerBank)) & ~7;
+    static constexpr int kMaxRegs = kMinBlocks == 2 ? 160 : kRegSplit > 255 ? 255 : kRegSplit;
+    static_assert(kMaxRegs <= kRegSplit || kRegSplit > 255, "the CTAs must fit in the register file");
     static constexpr int kHeader = 1024;                    // barriers and flags
     static constexpr int kMmaSteps = kRowBytes / 32;        // 32 bytes of K per tcgen05.mma
     static constexpr int kActScaleBytes = NPAD * 4;         // per cached K block
@@ -178,7 +196,7 @@ template <int NPAD, int MODE> struct GemmCfg {
 // GREEDY: the greedy-choice epilogue is compiled in (a separate instantiation,
 // so the plain layer carries none of its code).
 template <int NPAD, int MODE, bool GREEDY>
-__global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, MODE>::kMinBlocks)
+__global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     gemm_small_m_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p)
 {
@@ -595,7 +613,7 @@ __global__ void __launch_bounds__(GemmCfg<NPAD, MODE>::kThreads, GemmCfg<NPAD, M
                             const uint32_t nmin =
                                 __reduce_min_sync(0xffffffffu, key == kmax ? static_cast<uint32_t>(n) : 0xffffffffu);
                             if (lane == 0)
-                                atomicMax(&cta_best[m],
+                                atomicMax(&cta_best[col0 + m],
                                           (static_cast<unsigned long long>(kmax) << 32) | (0xffffffffu - nmin));
                         }
                     }

@@ -100,10 +100,14 @@ __global__ void __launch_bounds__(256) mx_quant_weight_kernel(const void *__rest
     }
 }
 
-// Activations: one CTA per 128-wide K group, warp w taking tokens w, w+8,
-// ... < 128.  Codes row-major [M][K]; the group's atom gets the scale bytes
-// of tokens < M and zeros for the other rows.
-__global__ void __launch_bounds__(256) mx_quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
+// Activations: one CTA of four warps per 128-wide K group (a CTA small
+// enough to sit beside the two CTAs of the 16-token GEMM).  The CTA first
+// zeroes the group's 512-byte atom (one word per thread), then warp w casts
+// tokens w, w+4, ... < M.  Codes row-major [M][K]; the atom ends with the
+// scale bytes of tokens < M and zeros for the other rows.
+constexpr int kMxCastWarps = 4;
+
+__global__ void __launch_bounds__(32 * kMxCastWarps) mx_quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
                                                            uint8_t *__restrict__ xq, uint8_t *__restrict__ sf,
                                                            unsigned long long *runs)
 {
@@ -114,19 +118,17 @@ __global__ void __launch_bounds__(256) mx_quant_act_kernel(const uint16_t *__res
     const int g = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *atom = sf + static_cast<long long>(g) * 512;
-    for (int m = warp; m < 128; m += 8) {
-        if (m < M) { // warp-uniform
-            const uint2 raw =
-                *reinterpret_cast<const uint2 *>(x + static_cast<long long>(m) * ldx + g * 128 + lane * 4);
-            uint32_t byte;
-            const uint32_t codes =
-                mx_quant_row128(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y), &byte);
-            *reinterpret_cast<uint32_t *>(xq + static_cast<long long>(m) * K + g * 128 + lane * 4) = codes;
-            if ((lane & 7) == 0)
-                atom[sf_atom_offset(m, lane >> 3)] = static_cast<uint8_t>(byte);
-        } else if ((lane & 7) == 0) {
-            atom[sf_atom_offset(m, lane >> 3)] = 0;
-        }
+    static_assert(32 * kMxCastWarps * 4 == 512, "one word of the atom per thread");
+    reinterpret_cast<uint32_t *>(atom)[threadIdx.x] = 0u;
+    __syncthreads(); // the zeros land before the scale bytes below
+    const int rows = M < 128 ? M : 128;
+    for (int m = warp; m < rows; m += kMxCastWarps) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(x + static_cast<long long>(m) * ldx + g * 128 + lane * 4);
+        uint32_t byte;
+        const uint32_t codes = mx_quant_row128(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y), &byte);
+        *reinterpret_cast<uint32_t *>(xq + static_cast<long long>(m) * K + g * 128 + lane * 4) = codes;
+        if ((lane & 7) == 0)
+            atom[sf_atom_offset(m, lane >> 3)] = static_cast<uint8_t>(byte);
     }
 }
 
@@ -148,7 +150,7 @@ fp8bs_status launch_mx_quant_act(const void *x, int M, int K, int ldx, uint8_t *
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(K / 128), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(32 * kMxCastWarps, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -20,7 +20,13 @@
 
 namespace fp8bs {
 
-__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
+// Activation cast: one warp per (token, 128-wide K group), four per CTA.  A
+// CTA this small (4,096 registers) fits on an SM beside the two CTAs of the
+// 16-token GEMM, so under programmatic dependent launch it never keeps the
+// next GEMM's early CTA off that SM.
+constexpr int kCastThreads = 128;
+
+__global__ void __launch_bounds__(kCastThreads) quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
                                                         uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                         unsigned long long *runs)
 {
@@ -29,7 +35,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t *__restri
     grid_launch_dependents();
     grid_dependency_wait();
     const int kg = K / 128;
-    const long long group = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const long long group = static_cast<long long>(blockIdx.x) * (kCastThreads / 32) + (threadIdx.x >> 5);
     if (group >= static_cast<long long>(M) * kg)
         return; // whole warp
     const int lane = threadIdx.x & 31;
@@ -113,8 +119,9 @@ fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq,
 {
     const long long groups = static_cast<long long>(M) * (K / 128);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((groups + 7) / 8), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    constexpr int kGroupsPerCta = kCastThreads / 32;
+    cfg.gridDim = dim3(static_cast<unsigned>((groups + kGroupsPerCta - 1) / kGroupsPerCta), 1, 1);
+    cfg.blockDim = dim3(kCastThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -158,13 +158,15 @@ def test_split_plan_partitions_units(L):
 def test_gemm_schedule_policy(L):
     """The schedule for M tokens: up to 64 tokens one token tile and K split
     over every SM; above, whole (token tile, weight tile) pairs per CTA when
-    they occupy at least half of the SMs, stream-K over 128-token pairs
-    otherwise (when the pairs cover every SM, or when N is too small)."""
+    they fit in one wave and leave at most a 16/kg fraction of the SMs idle,
+    stream-K over 128-token pairs otherwise (always when the 128-token pairs
+    cover every SM)."""
     def tpad(M):
         return 16 if M <= 16 else 32 if M <= 32 else 48 if M <= 48 else 64
     for sms in (152, 148, 160):
         for M in (1, 8, 16, 17, 33, 64, 65, 100, 128, 129, 256, 300, 384, 512):
-            for N, K in ((5120, 5120), (34816, 5120), (5120, 17408), (640, 1024), (300, 256), (128, 128)):
+            for N, K in ((5120, 5120), (7168, 5120), (34816, 5120), (5120, 17408), (640, 1024), (300, 256),
+                         (128, 128)):
                 s = fb.gemm_schedule(M, N, K, sms)
                 ntiles, kg = (N + 127) // 128, K // 128
                 assert s["units"] == s["token_tiles"] * ntiles * kg
@@ -173,15 +175,27 @@ def test_gemm_schedule_policy(L):
                     assert (s["npad"], s["token_tiles"], s["split"]) == (tpad(M), 1, True)
                     assert s["ctas"] == min(s["units"], sms)
                 elif not s["split"]:
+                    pairs = s["ctas"]
                     assert s["npad"] in (32, 64, 128)
-                    assert s["ctas"] == s["token_tiles"] * ntiles and 2 * s["ctas"] >= sms
+                    assert pairs == s["token_tiles"] * ntiles and pairs <= sms
+                    assert pairs * (kg + 16) >= sms * kg, "too many idle SMs for an unsplit K"
                     assert ntiles * ((M + 127) // 128) < sms, "pairs cover the SMs: stream-K expected"
+                    # the widest token tile that qualifies
+                    for wider in (128, 64):
+                        if wider > s["npad"]:
+                            p2 = ntiles * ((M + wider - 1) // wider)
+                            assert not (p2 <= sms and p2 * (kg + 16) >= sms * kg)
                 else:
                     assert s["npad"] == 128 and s["ctas"] == min(s["units"], sms)
-    sq = lambda M: fb.gemm_schedule(M, 5120, 5120, 152)
-    assert sq(512) == dict(npad=128, token_tiles=4, ctas=152, units=6400, split=True)
-    assert sq(256) == dict(npad=128, token_tiles=2, ctas=80, units=3200, split=False)
-    assert sq(8) == dict(npad=16, token_tiles=1, ctas=152, units=1600, split=True)
+    sched = lambda M, N, K: fb.gemm_schedule(M, N, K, 152)
+    assert sched(512, 5120, 5120) == dict(npad=128, token_tiles=4, ctas=152, units=6400, split=True)
+    # 80 pairs of a short K, 80 of a long K: both stream-K
+    assert sched(256, 5120, 5120) == dict(npad=128, token_tiles=2, ctas=152, units=3200, split=True)
+    assert sched(128, 5120, 17408) == dict(npad=128, token_tiles=1, ctas=152, units=5440, split=True)
+    # 112 pairs of a 40-block K: one CTA per pair
+    assert sched(256, 7168, 5120) == dict(npad=128, token_tiles=2, ctas=112, units=4480, split=False)
+    assert sched(128, 7168, 5120) == dict(npad=64, token_tiles=2, ctas=112, units=4480, split=False)
+    assert sched(8, 5120, 5120) == dict(npad=16, token_tiles=1, ctas=152, units=1600, split=True)
     with pytest.raises(fb.Fp8bsError):
         fb.gemm_schedule(513, 5120, 5120, 152)
 
