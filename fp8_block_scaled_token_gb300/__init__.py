@@ -159,8 +159,16 @@ def _rows_contiguous(t, name):
 
 
 # ---------------------------------------------------------------- entry points
+def scales_shape(M, K):
+    """Shape of the activation scales for M tokens: (M, K/128) token-major up
+    to 16 tokens, (K/128, M) K-block-major above."""
+    kg = max(K // 128, 0)
+    return (M, kg) if M <= 16 else (kg, M)
+
+
 def fp8_quant_act(x, xq=None, xs=None, flags=0):
-    """bf16 X [M, K] (row stride may exceed K) -> (xq uint8 [M,K], xs fp32 [M,K/128])."""
+    """bf16 X [M, K] (row stride may exceed K) -> (xq uint8 [M,K], xs fp32 of
+    scales_shape(M, K))."""
     torch = _torch()
     _need(x, torch.bfloat16, "x")
     _rows_contiguous(x, "x")
@@ -168,7 +176,7 @@ def fp8_quant_act(x, xq=None, xs=None, flags=0):
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if xs is None:
-        xs = torch.empty((M, max(K // 128, 0)), dtype=torch.float32, device=x.device)
+        xs = torch.empty(scales_shape(M, K), dtype=torch.float32, device=x.device)
     _check("fp8_quant_act", lib().fp8_quant_act(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(xs), flags, _stream()))
     return xq, xs
 
@@ -258,7 +266,7 @@ def fp8_blockscaled_gemm(aq, as_, wq, ws, y=None, workspace=None, flags=0, n=Non
     M, K = aq.shape
     N, tf = _weight_dims(wq, K, n, "wq")
     flags |= tf
-    if tuple(as_.shape) != (M, K // 128) or tuple(ws.shape) != ((N + 127) // 128, K // 128):
+    if tuple(as_.shape) != scales_shape(M, K) or tuple(ws.shape) != ((N + 127) // 128, K // 128):
         raise ValueError("operand shapes do not agree")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)

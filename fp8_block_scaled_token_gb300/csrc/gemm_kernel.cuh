@@ -78,7 +78,7 @@ struct GemmParams {
     int ctas;
     int stages;      // ring depth, <= kMaxStages
     int act_chunks;  // fused: K blocks in the activation cache (>= distinct K blocks of any CTA)
-    const float *as;         // FP8: s_a [M][K/128]
+    const float *as;         // FP8: s_a [M][K/128] (M <= 16) or [K/128][M] (M > 16)
     const float *ws;         // FP8: s_w [ntiles][K/128]
     const uint8_t *sfa;      // MX: weight scale atoms [ntiles][K/128][512]
     const uint8_t *sfb;      // MX: activation scale atoms [K/128][512]
@@ -158,13 +158,25 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kColGroups = NPAD >= 64 ? 2 : 1;
     static constexpr int kCols = NPAD / kColGroups;         // token columns per epilogue thread
     static constexpr int kEpiWarps = 4 * kColGroups;
-    // From 32 tokens up, the per-unit scale products s_w * s_a[m] are formed
-    // once per token and read back from shared memory (four per load), which
-    // removes a shuffle and a multiply per token per weight row.  The 16-token
-    // tile (decode) keeps the per-lane scales and shuffles: there the extra
+    // From 32 tokens up, the per-unit scale products s_w * s_a[m] of a
+    // warp's token columns are formed by the warp itself (each lane one or
+    // two tokens, their scales one coalesced load apiece from the
+    // K-block-major activation scales) into its own shared-memory slot and
+    // read back four per load, which removes a shuffle and a multiply per
+    // token per weight row.  A __syncwarp publishes them: no barrier across
+    // the epilogue warps in the per-unit loop (measured against products
+    // formed once per token and published by such a barrier: 128-token tiles
+    // 6-11% faster per layer, 32- and 64-token tiles 2%).  The 16-token tile
+    // (decode) keeps the per-lane scales and shuffles: there the extra
     // shared-memory round trip on the per-unit critical path cost ~0.2 us.
+    // The activation-scale layout goes with M: token-major [M][K/128] up to
+    // 16 tokens, K-block-major [K/128][M] above (the cast writes it so); the
+    // schedule gives exactly those M the 16-token tile, so each
+    // instantiation reads one fixed layout (a run-time choice in this loop
+    // cost 3 % at decode sizes).
     static constexpr bool kProducts = NPAD >= 32 && !kTileAcc;
-    static constexpr int kProdBytes = kProducts ? 2 * NPAD * 4 : 0; // double-buffered
+    static constexpr int kProdPerLane = (kCols + 31) / 32; // token columns per lane
+    static constexpr int kProdBytes = kProducts ? kEpiWarps * 2 * kCols * 4 : 0; // per warp, by unit parity
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kQuantWarps);
     // Registers per thread.  An SM's register file is four 16,384-register
     // banks, one per scheduler, and a CTA's warps are spread over the four:
@@ -225,7 +237,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     uint8_t *ring = smem + C::kHeader;
     uint8_t *act_cache = ring + S * C::kStageBytes;
     float *act_scale = reinterpret_cast<float *>(act_cache + p.act_chunks * C::kBBytes);
-    float *prod = act_scale + p.act_chunks * NPAD; // [2][NPAD] s_w * s_a of the current units
+    float *prod = act_scale + p.act_chunks * NPAD; // [epilogue warp][2][kCols] s_w * s_a
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -620,21 +632,32 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                 }
             };
             // Scales of the next unit to promote, loaded one unit ahead by
-            // the thread of each token (thread index tpr < NPAD).
-            const int tpr = threadIdx.x - 64;
-            float nx_sw = 0.0f, nx_sa = 0.0f;
+            // every lane for its token columns col0 + lane + 32 q of the tile
+            // (the activation scales are K-block-major above 16 tokens: the
+            // lanes' loads are consecutive words).
+            float nx_sw = 0.0f, nx_sa[C::kProdPerLane];
+#pragma unroll
+            for (int q = 0; q < C::kProdPerLane; ++q)
+                nx_sa[q] = 0.0f;
             auto load_scales = [&](int wtl, int ttl, int kbb, int sl) {
                 if (!FP8BS_CHECK(wtl >= 0 && wtl < p.ntiles && kbb >= 0 && kbb < kg &&
                                  (MODE != kModeFp8Fused || (sl >= 0 && sl < p.act_chunks))))
                     return;
                 nx_sw = p.ws[static_cast<long long>(wtl) * kg + kbb];
-                if (MODE == kModeFp8) {
-                    const int tok = ttl * NPAD + tpr;
-                    nx_sa = tok < p.M ? p.as[static_cast<long long>(tok) * kg + kbb] : 0.0f;
-                } else {
-                    nx_sa = act_scale[sl * NPAD + tpr]; // zero for rows >= M
+#pragma unroll
+                for (int q = 0; q < C::kProdPerLane; ++q) {
+                    const int t = col0 + lane + 32 * q; // column within the token tile
+                    const bool col_ok = lane + 32 * q < C::kCols;
+                    if (MODE == kModeFp8) {
+                        // 32 tokens and wider: M > 16, K-block-major scales
+                        const int tok = ttl * NPAD + t;
+                        nx_sa[q] = (col_ok && tok < p.M) ? p.as[static_cast<long long>(kbb) * p.M + tok] : 0.0f;
+                    } else {
+                        nx_sa[q] = col_ok ? act_scale[sl * NPAD + t] : 0.0f; // zero for rows >= M
+                    }
                 }
             };
+            float *const wprod = prod + (warp - 2) * 2 * C::kCols; // this warp's [2][kCols]
             // 16-token tile: the weight-block scale of the next unit and
             // (pre-quantised activations) each lane's token scale, loaded one
             // unit ahead so no global load sits between a finished MMA and
@@ -646,14 +669,14 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                     return;
                 nx16_sw = p.ws[static_cast<long long>(wtl) * kg + kbb];
                 if (MODE == kModeFp8 && lane < mcnt)
-                    nx16_sa = p.as[static_cast<long long>(tok0 + lane) * kg + kbb];
+                    nx16_sa = p.as[static_cast<long long>(tok0 + lane) * kg + kbb]; // M <= 16: token-major
             };
             // Everything above is local set-up (split plans, unit state); the
             // first read of data the previous grid may write comes next, so
             // the dependency wait sits here (decode layer 11.57 -> 11.32 us).
             if constexpr (MODE != kModeFp8Fused)
                 grid_dependency_wait();
-            if (C::kProducts && tpr < NPAD && nunits > 0)
+            if (C::kProducts && nunits > 0)
                 load_scales(wt, ttile, kb, slot);
             if (kLaneScales && nunits > 0)
                 load_scales16(wt, kb);
@@ -678,15 +701,19 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                 if (seg_start)
                     seg_first_kb = kb;
                 if (!C::kTileAcc || seg_end) {
-                    // One thread per token forms s_w * s_a for this unit from
-                    // the scales it loaded one unit ahead, and loads the next
-                    // unit's; the barrier below publishes the products
-                    // (double-buffered by unit parity: a buffer is rewritten
-                    // only after every thread has passed the next unit's
-                    // barrier).
-                    float *pr = prod + (i & 1) * NPAD;
-                    if (C::kProducts && tpr < NPAD) {
-                        pr[tpr] = nx_sw * nx_sa;
+                    // Each lane forms s_w * s_a of its token columns for this
+                    // unit from the scales it loaded one unit ahead, and
+                    // loads the next unit's; the __syncwarp publishes the
+                    // warp's products (double-buffered by unit parity: a
+                    // buffer is rewritten only after every lane has passed
+                    // the next unit's __syncwarp).
+                    float *pr = wprod + (i & 1) * C::kCols;
+                    if constexpr (C::kProducts) {
+#pragma unroll
+                        for (int q = 0; q < C::kProdPerLane; ++q)
+                            if (lane + 32 * q < C::kCols)
+                                pr[lane + 32 * q] = nx_sw * nx_sa[q];
+                        __syncwarp();
                         if (i + 1 < nunits) {
                             const bool wrap = kb + 1 == kg;
                             const bool wrap_w = !kOneTT && wrap && wt + 1 == p.ntiles;
@@ -706,15 +733,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                     const bool slot_ok = MODE != kModeFp8Fused || FP8BS_CHECK(slot >= 0 && slot < p.act_chunks);
                     const float *sa_c = act_scale + (MODE == kModeFp8Fused && slot_ok ? slot * NPAD : 0) + col0;
                     mbar_wait(&tfull[accb], acc_ph, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
-                    if constexpr (C::kProducts) {
-                        // The barrier publishes the products written above.  Its
-                        // reduction also gives every epilogue thread one answer
-                        // on the abort flag, which another warp may raise at
-                        // any moment.
-                        if (named_bar_any(1, 32 * C::kEpiWarps, *abort_flag != 0))
-                            break;
-                    }
-                    // Without a barrier here, a thread whose wait gave up
+                    // No barrier here: a thread whose wait gave up
                     // (abort) carries on through the remaining units and the
                     // exchange with whatever the accumulator holds: every
                     // later wait gives up after its next look at the abort
@@ -739,8 +758,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                         if constexpr (C::kProducts) {
 #pragma unroll
                             for (int q = 0; q < kLd / 4; ++q)
-                                *reinterpret_cast<float4 *>(&sc[4 * q]) =
-                                    reinterpret_cast<const float4 *>(pr + col0 + c * kLd)[q];
+                                *reinterpret_cast<float4 *>(&sc[4 * q]) = reinterpret_cast<const float4 *>(pr + c * kLd)[q];
                         } else if constexpr (!C::kTileAcc) {
 #pragma unroll
                             for (int j = 0; j < kLd; ++j)

@@ -401,21 +401,5 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Named barrier that also returns, to every participating thread, whether
-// any of them passed `pred` true: one decision all of them share, even when
-// the value behind `pred` changes while they arrive.
-__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t nthreads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %3, 0;\n\t"
-        "bar.red.or.pred po, %1, %2, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(id), "r"(nthreads), "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return r != 0;
-}
 
 } // namespace fp8bs

@@ -26,6 +26,11 @@ namespace fp8bs {
 // next GEMM's early CTA off that SM.
 constexpr int kCastThreads = 128;
 
+// kKMajor (M > 16): the scales are written K-block-major ([K/128][M], the
+// layout the GEMM reads above 16 tokens) rather than token-major
+// ([M][K/128]); a separate instantiation each, so the token-major one's code
+// is the same as if the other did not exist.
+template <bool kKMajor>
 __global__ void __launch_bounds__(kCastThreads) quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
                                                         uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                         unsigned long long *runs)
@@ -39,14 +44,16 @@ __global__ void __launch_bounds__(kCastThreads) quant_act_kernel(const uint16_t 
     if (group >= static_cast<long long>(M) * kg)
         return; // whole warp
     const int lane = threadIdx.x & 31;
-    const int m = static_cast<int>(group / kg);
-    const int g = static_cast<int>(group % kg);
+    // groups in the order of the scales they write: a CTA's warps then store
+    // consecutive scale words
+    const int m = static_cast<int>(kKMajor ? group % M : group / kg);
+    const int g = static_cast<int>(kKMajor ? group / M : group % kg);
     const uint2 raw = *reinterpret_cast<const uint2 *>(x + static_cast<long long>(m) * ldx + g * 128 + lane * 4);
     uint32_t codes;
     const float s = quant_group_warp(raw, codes);
     *reinterpret_cast<uint32_t *>(xq + static_cast<long long>(m) * K + g * 128 + lane * 4) = codes;
     if (lane == 0)
-        xs[static_cast<long long>(m) * kg + g] = s;
+        xs[kKMajor ? static_cast<long long>(g) * M + m : static_cast<long long>(m) * kg + g] = s;
 }
 
 // kTiled: write the codes of block (nb, kb) as one contiguous 16 KB run
@@ -129,7 +136,8 @@ fp8bs_status launch_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return launch_status(cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const uint16_t *>(x), M, K, ldx,
+    return launch_status(cudaLaunchKernelEx(&cfg, M > 16 ? quant_act_kernel<true> : quant_act_kernel<false>,
+                                            static_cast<const uint16_t *>(x), M, K, ldx,
                                             xq, xs, dev.runs));
 }
 

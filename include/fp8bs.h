@@ -31,9 +31,13 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the
  *     library allocates no device memory and keeps no pointer after return.
- *   - Row-major layouts: X bf16 [M][ldx]; Aq u8 [M][K]; s_a fp32 [M][K/128];
- *     W fp32|bf16 [N][K]; Wq u8 [N][K]; s_w fp32 [ceil(N/128)][K/128];
- *     Y bf16 [M][N].
+ *   - Row-major layouts: X bf16 [M][ldx]; Aq u8 [M][K]; W fp32|bf16 [N][K];
+ *     Wq u8 [N][K]; s_w fp32 [ceil(N/128)][K/128]; Y bf16 [M][N].
+ *   - Activation scales s_a (fp32, M*(K/128) words): token-major [M][K/128]
+ *     (element m*(K/128) + g) when M <= 16, K-block-major [K/128][M]
+ *     (element g*M + m) when M > 16; the two coincide at M = 1.  Each is the
+ *     faster one for the GEMM at that size: above 16 tokens the epilogue
+ *     loads one K block's scales for a warp's tokens with one request.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
  *     enqueued asynchronously; no call synchronises the host except
  *     fp8bs_workspace_status().
@@ -99,10 +103,12 @@ FP8BS_API const char *fp8bs_status_string(fp8bs_status status);
  * Activation quantisation [P2 "What the trace showed"; P3 "Quantisation
  * kernels"].  For every token m and every group g of 128 consecutive K:
  *   amax = max |x[m, 128g .. 128g+127]|
- *   xs[m*(K/128) + g] = amax == 0 ? 1.0f : fl32(amax / 448)
- *   xq[m*K + k]       = e4m3_rn_satfinite(fl32(x[m,k] / xs[m, k/128]))
+ *   s(m, g)     = amax == 0 ? 1.0f : fl32(amax / 448)
+ *   xq[m*K + k] = e4m3_rn_satfinite(fl32(x[m,k] / s(m, k/128)))
+ * with s(m, g) stored at xs[m*(K/128) + g] when M <= 16 and at xs[g*M + m]
+ * when M > 16 (the activation-scale layouts above).
  * x : bf16, M rows, row stride ldx elements; 16-byte aligned, ldx % 8 == 0.
- * xq: u8 [M][K], 4-byte aligned.  xs: fp32 [M][K/128], 4-byte aligned.
+ * xq: u8 [M][K], 4-byte aligned.  xs: fp32, M*(K/128) words, 4-byte aligned.
  * M >= 1, K >= 128, K % 128 == 0, ldx >= K.
  * Any `flags` value other than 0 and FP8BS_FLAG_OVERLAP_PREV is rejected;
  * with the flag the kernel is launched with programmatic dependent launch and
@@ -159,7 +165,8 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, 
  * Swap-AB tcgen05 kernel (weights in the MMA M dimension, tokens in N),
  * 128x128 weight tiles streamed by TMA, K split across every SM with a
  * fixed-order reduction.
- * aq: u8 [M][K], 16-byte aligned.   as: fp32 [M][K/128].
+ * aq: u8 [M][K], 16-byte aligned.   as: fp32, laid out as fp8_quant_act writes
+ * it for this M ([M][K/128] up to 16 tokens, [K/128][M] above).
  * wq: u8 [N][K], 16-byte aligned.   ws: fp32 [ceil(N/128)][K/128].
  * y : bf16 [M][N], 2-byte aligned.
  * 1 <= M <= 512, N >= 1, K >= 128, K % 128 == 0.  Up to 64 tokens the
