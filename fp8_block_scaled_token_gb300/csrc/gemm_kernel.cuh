@@ -133,7 +133,15 @@ template <int NPAD, int MODE> struct GemmCfg {
     // per-K-block scale to apply on CUDA cores).
     static constexpr bool kTileAcc = MODE == kModeBf16 || kMx;
     static constexpr int kMaxStages = 12;
-    static constexpr int kAcc = NPAD == 256 ? 2 : 4;       // TMEM holds 512 fp32 columns
+    // Accumulators in tensor memory (512 fp32 columns per SM, two CTAs of
+    // the 16-token tile sharing them): eight for the 16-token tile, so the
+    // MMA runs up to eight units ahead of an epilogue that stalls (for
+    // instance ~1.3 us on a release-ordered arrival issued while every SM
+    // streams weights); four otherwise.  Measured on the decode pass (two
+    // libraries alternating in one process, three boxes): eight against four
+    // 1.2-1.6 % faster at M = 1 and 8; sixteen 0.3 % slower than eight; eight
+    // for the 32- to 64-token tiles within +-0.7 % (not taken).
+    static constexpr int kAcc = NPAD == 16 ? 8 : NPAD == 256 ? 2 : 4;
     // MX: after the accumulators, 8 columns of scale factors per ring stage
     // (4 for the weight atom, 4 for the token atom).
     static constexpr int kSfCol = kAcc * NPAD;
@@ -192,6 +200,8 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kMaxRegs = kMinBlocks == 2 ? 160 : kRegSplit > 255 ? 255 : kRegSplit;
     static_assert(kMaxRegs <= kRegSplit || kRegSplit > 255, "the CTAs must fit in the register file");
     static constexpr int kHeader = 1024;                    // barriers and flags
+    // the mbarriers, the TMEM address and two flags end below the greedy keys at 512
+    static_assert((2 * kMaxStages + 2 * kAcc + 2) * 8 + 12 <= 512, "header layout");
     static constexpr int kMmaSteps = kRowBytes / 32;        // 32 bytes of K per tcgen05.mma
     static constexpr int kActScaleBytes = NPAD * 4;         // per cached K block
     static constexpr uint32_t kIdesc =
