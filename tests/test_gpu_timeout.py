@@ -26,8 +26,16 @@ def _stall(xq, xs, wq, ws, y, M, N, K, work, skip_unit, timeout_ns):
         ctypes.c_void_p(work.data_ptr()), work.numel(), skip_unit, timeout_ns, stream)
 
 
-@pytest.mark.parametrize("M,N,K,skip", [(8, 256, 512, 0), (8, 5120, 5120, 3)])
+# 16-token tile (decode), and the wider tiles whose epilogue forms its scale
+# products per warp with no barrier across the epilogue warps: after the
+# time-out every epilogue warp must still run through its units and meet the
+# exchange's barriers, and the CTA must still free its tensor memory.
+@pytest.mark.parametrize("M,N,K,skip", [(8, 256, 512, 0), (8, 5120, 5120, 3), (33, 5120, 5120, 2),
+                                        (128, 5120, 5120, 5), (512, 384, 512, 1)])
 def test_bounded_wait_reports_timeout_and_context_survives(M, N, K, skip):
+    # the skipped unit index is per CTA: every CTA must have more units than that
+    sched = fb.gemm_schedule(M, N, K)
+    assert sched["units"] // sched["ctas"] > skip
     x = synth.activations(M, K, seed=5)
     w = synth.weights(N, K, seed=6)
     xd, wd = x.cuda(), w.cuda()
