@@ -201,7 +201,7 @@ template <int NPAD, int MODE> struct GemmCfg {
     static_assert(kMaxRegs <= kRegSplit || kRegSplit > 255, "the CTAs must fit in the register file");
     static constexpr int kHeader = 1024;                    // barriers and flags
     // the mbarriers, the TMEM address and two flags end below the greedy keys at 512
-    static_assert((2 * kMaxStages + 2 * kAcc + 2) * 8 + 12 <= 512, "header layout");
+    static_assert((2 * kMaxStages + 2 * kAcc + 3) * 8 + 12 <= 512, "header layout");
     static constexpr int kMmaSteps = kRowBytes / 32;        // 32 bytes of K per tcgen05.mma
     static constexpr int kActScaleBytes = NPAD * 4;         // per cached K block
     static constexpr uint32_t kIdesc =
@@ -239,7 +239,8 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     uint64_t *tempty = tfull + C::kAcc;
     uint64_t *mma_done = tempty + C::kAcc;
     uint64_t *act_ready = mma_done + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(act_ready + 1);
+    uint64_t *red_ready = act_ready + 1; // bulk copies of the exchange slots (last segment)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
     unsigned long long *cta_best = reinterpret_cast<unsigned long long *>(smem + 512); // [64] greedy keys
@@ -272,6 +273,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
         }
         mbar_init(mma_done, 1);
         mbar_init(act_ready, 1);
+        mbar_init(red_ready, 1);
         *abort_flag = 0;
         *last_flag = 0;
     }
@@ -597,6 +599,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
             int accb = 0;
             uint32_t acc_ph = 0;
             int seg_first_kb = 0;
+            bool bulk_issued = false; // warp 2 lane 0: slot copies into the ring
             int tile = static_cast<int>(u0 / kg), kb = kb0, slot = 0;
             // Reduction plans of the (at most two) tiles this CTA may share:
             // the tile its range starts in and the one it ends in.  Worked out
@@ -827,12 +830,45 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
 #pragma unroll
                         for (int m = 0; m < C::kCols; ++m)
                             acc[m] = 0.0f;
-                        // Issue every contributor's loads for a chunk of tokens at
-                        // once (one L2 round trip per chunk), then add them in
-                        // contributor order.
+                        // From 32 tokens up, at the range's last segment: every
+                        // unit's MMAs are done, so the weight ring is idle and
+                        // each contributor's whole slot (16 to 64 KB) comes in
+                        // with one bulk copy, all in one round trip; the sums
+                        // then read shared memory, in contributor order as
+                        // below.  (Through registers a thread keeps two to six
+                        // contributors' 8 to 32 columns in flight at a time:
+                        // several sequential round trips per tile.  The 16-token
+                        // tile's partials take one round trip that way.)
+                        constexpr int kSlotBytes = NPAD * 128 * 4;
+                        const int ncon = c_last - c_first + 1;
+                        const bool bulk = NPAD >= 32 && i == nunits - 1 &&
+                                          static_cast<long long>(ncon) * kSlotBytes <= static_cast<long long>(S) * C::kStageBytes;
+                        if (bulk) {
+                            if (warp == 2 && lane == 0) {
+                                fence_proxy_async_global(); // the partials were stored by generic writes
+                                mbar_arrive_expect_tx(red_ready, static_cast<uint32_t>(ncon * kSlotBytes));
+                                const uint64_t pol = l2_policy_evict_first();
+                                for (int j = 0; j < ncon; ++j)
+                                    if (FP8BS_CHECK(slot_of(c_first + j) < 2 * p.ctas))
+                                        bulk_load_1d(ring + j * kSlotBytes,
+                                                     slots_y + static_cast<long long>(slot_of(c_first + j)) * (NPAD * 128),
+                                                     kSlotBytes, red_ready, pol);
+                                bulk_issued = true;
+                            }
+                            mbar_wait(red_ready, 0, abort_flag, p.status, kErrTimeoutEpilogue, p.timeout_ns);
+                            const float *sm = reinterpret_cast<const float *>(ring) + col0 * 128 + row;
+                            for (int j = 0; j < ncon; ++j)
+#pragma unroll
+                                for (int m = 0; m < C::kCols; ++m)
+                                    if (m < mcnt)
+                                        acc[m] += sm[j * (NPAD * 128) + m * 128];
+                        }
+                        // Otherwise issue every contributor's loads for a chunk of
+                        // tokens at once (one L2 round trip per chunk), then add
+                        // them in contributor order.
                         constexpr int kMaxC = NPAD > 64 ? 2 : 6;
                         constexpr int kMC = NPAD <= 16 ? 16 : NPAD > 64 ? 32 : 8;
-                        for (int c0 = c_first; c0 <= c_last; c0 += kMaxC) {
+                        for (int c0 = bulk ? c_last + 1 : c_first; c0 <= c_last; c0 += kMaxC) {
                             const int nc = c_last - c0 + 1 < kMaxC ? c_last - c0 + 1 : kMaxC;
                             const float *src[kMaxC];
 #pragma unroll
@@ -866,6 +902,18 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
 #pragma unroll
                 for (int m = 0; m < C::kCols; ++m)
                     acc[m] = 0.0f;
+            }
+            // The slot copies must have landed before the CTA exits, also when
+            // the wait above gave up (abort): a bounded wait of the thread that
+            // issued them.
+            if (bulk_issued) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_test(red_ready, 0)) {
+                    if (globaltimer_ns() - t0 > p.timeout_ns) {
+                        atomicOr(p.status, kErrTimeoutEpilogue);
+                        break;
+                    }
+                }
             }
             if constexpr (GREEDY) {
                 // ---- greedy: publish this CTA's keys; the last CTA finishes
