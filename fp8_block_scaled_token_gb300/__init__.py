@@ -33,6 +33,7 @@ DEBUG_LIB_PATH = os.path.join(PKG, "lib", "libfp8bs_debug.so")
 
 FLAG_OVERLAP_PREV = 1
 FLAG_WEIGHTS_TILED = 2
+FLAG_PROLOGUE_CAST = 4
 F32, BF16 = 0, 1
 
 _lib = None
@@ -95,7 +96,7 @@ def _load(path):
                              ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)],
         "fp8bs_gemm_schedule": [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i), ctypes.POINTER(i),
                                 ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(i)],
-        "fp8bs_fused_route": [i, i, i, i, ctypes.POINTER(i)],
+        "fp8bs_fused_route": [i, i, i, i, ctypes.c_uint, ctypes.POINTER(i)],
         "fp8bs_testhook_gemm_stall": [vp, vp, vp, vp, vp, i, i, i, vp, sz, i, ctypes.c_ulonglong, vp],
         "fp8bs_testhook_kernel_runs": [i, i, ctypes.POINTER(ctypes.c_ulonglong)],
         "fp8bs_testhook_gemm_fused_sms": [vp, i, vp, vp, vp, i, i, i, vp, sz, u, i, vp],
@@ -445,12 +446,12 @@ def split_plan(N, K, bf16=False, num_sms=0, cta=-1):
     return c.value, u.value, (b.value if cta >= 0 else None), (e.value if cta >= 0 else None)
 
 
-def fused_route(M, N, K, num_sms=0):
+def fused_route(M, N, K, num_sms=0, flags=0):
     """'prologue' when fp8_blockscaled_gemm_fused casts the activations in the
-    GEMM kernel's prologue for this shape, 'separate' when it runs the cast as
-    its own kernel first."""
+    GEMM kernel's prologue for this shape and flags (FLAG_PROLOGUE_CAST, where
+    the cache fits), 'separate' when it runs the cast as its own kernel first."""
     v = ctypes.c_int(0)
-    _check("fp8bs_fused_route", lib().fp8bs_fused_route(M, N, K, num_sms, ctypes.byref(v)))
+    _check("fp8bs_fused_route", lib().fp8bs_fused_route(M, N, K, num_sms, flags, ctypes.byref(v)))
     return "prologue" if v.value else "separate"
 
 

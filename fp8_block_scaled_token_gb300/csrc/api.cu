@@ -212,6 +212,7 @@ fp8bs_status check_flags(unsigned flags, unsigned allowed)
 }
 
 constexpr unsigned kGemmFlags = FP8BS_FLAG_OVERLAP_PREV | FP8BS_FLAG_WEIGHTS_TILED;
+constexpr unsigned kFusedFlags = kGemmFlags | FP8BS_FLAG_PROLOGUE_CAST; // the fused entry points
 
 fp8bs_status quant_weight_common(const void *w, fp8bs_dtype wtype, int N, int K, uint8_t *wq, float *ws,
                                  bool tiled, void *stream)
@@ -407,7 +408,7 @@ fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx, const uint8_t *w
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
-    if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
+    if (ldx < K || check_flags(flags, kFusedFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||
         !aligned(workspace, 256))
@@ -443,7 +444,7 @@ fp8bs_status fp8_blockscaled_gemm_fused_greedy(const void *x, int ldx, const uin
         return st;
     if (M > 64)
         return FP8BS_ERR_UNSUPPORTED_SHAPE; // one greedy key per token, at most 64
-    if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
+    if (ldx < K || check_flags(flags, kFusedFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||
         !aligned(token, 4) || !aligned(logit, 4) || !aligned(workspace, 256))
@@ -658,9 +659,9 @@ fp8bs_status fp8_mx_gemm(const uint8_t *aq, const uint8_t *as_atoms, const uint8
     return run_gemm(L);
 }
 
-fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, int *prologue)
+fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, unsigned flags, int *prologue)
 {
-    if (!prologue)
+    if (!prologue || check_flags(flags, kFusedFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     *prologue = 0;
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
@@ -674,7 +675,7 @@ fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, int *prologue)
             return st;
         sms = dev.sms;
     }
-    *prologue = fused_prologue_route(gemm_shape(1, M, N, K, sms)) ? 1 : 0;
+    *prologue = fused_prologue_route(gemm_shape(1, M, N, K, sms), flags) ? 1 : 0;
     return FP8BS_OK;
 }
 
@@ -742,7 +743,7 @@ extern "C" fp8bs_status fp8bs_testhook_gemm_fused_sms(const void *x, int ldx, co
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
-    if (ldx < K || check_flags(flags, kGemmFlags) != FP8BS_OK)
+    if (ldx < K || check_flags(flags, kFusedFlags) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(wq, 16) || !aligned(ws, 4) || !aligned(y, 2) ||
         !aligned(workspace, 256))

@@ -6,15 +6,15 @@
 
 namespace fp8bs {
 
-bool fused_prologue_route(const GemmShape &sh)
+bool fused_prologue_route(const GemmShape &sh, unsigned flags)
 {
-    return fused_cache_fits<kModeFp8Fused>(sh);
+    return (flags & FP8BS_FLAG_PROLOGUE_CAST) != 0 && fused_cache_fits<kModeFp8Fused>(sh);
 }
 
 fp8bs_status launch_gemm_fused(const GemmLaunch &L, const DeviceInfo &dev)
 {
     const GemmShape sh = gemm_shape(kModeFp8Fused, L.M, L.N, L.K, L.sms > 0 ? L.sms : dev.sms);
-    if (fused_prologue_route(sh))
+    if (fused_prologue_route(sh, L.flags))
         return launch_gemm_mode<kModeFp8Fused>(L, dev);
     const WorkspaceLayout wl = workspace_layout(sh, L.M, L.K);
     uint8_t *aq = static_cast<uint8_t *>(L.workspace) + wl.act_off;

@@ -12,12 +12,14 @@ constexpr int kSmemLimit = 227 * 1024;      // dynamic shared memory per CTA
 constexpr int kRingBudget = 200 * 1024;     // ring of a kernel that has the SM to itself
 constexpr int kSharedRingBudget = 100 * 1024; // ring of a kernel that runs two CTAs per SM
 constexpr int kActCacheBudget = 96 * 1024;  // fused: activation cache + scales
-// fused: above this many (K block, token) rows per CTA the prologue cast costs
-// more than a separate cast kernel: the prologue can only start once the
-// previous kernel has produced the activations, and every CTA repeats it for
-// its own K blocks, while the separate kernel casts each row once and the
-// GEMM streams weights meanwhile.  Measured on GB300 (5,120^2 at M = 8:
-// 13.9 us with the prologue, 11.9 us with the separate kernel; equal at M = 1).
+// fused, FP8BS_FLAG_PROLOGUE_CAST: the prologue cast is taken only up to this
+// many (K block, token) rows per CTA.  It can only start once the previous
+// kernel has produced the activations, and every CTA repeats it for its own
+// K blocks, while the separate kernel casts each row once and the GEMM
+// (two CTAs per SM at 16 tokens) streams weights meanwhile.  Measured on
+// GB300, the separate cast was the faster route for every shape tried, from
+// 2 to 88 rows per CTA (5,120^2 at M = 8: 13.9 us with the prologue, 11.9 us
+// without; 1 to 16 tokens, 2 to 16 rows: 3-10 % in chains), hence opt-in.
 constexpr int kPrologueMaxRows = 16;
 
 // Ring depth and activation-cache size of a launch; act_chunks < 0 means the

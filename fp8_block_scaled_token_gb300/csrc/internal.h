@@ -91,8 +91,9 @@ struct GemmShape {
 GemmShape gemm_shape(int mode, int M, int N, int K, int sms);
 
 // True when the fused entry point casts the activations in the GEMM
-// prologue for this schedule; false when it runs the separate cast kernel.
-bool fused_prologue_route(const GemmShape &sh);
+// prologue for this schedule and flags (FP8BS_FLAG_PROLOGUE_CAST, and the
+// cache fits); false when it runs the separate cast kernel.
+bool fused_prologue_route(const GemmShape &sh, unsigned flags);
 
 // Device address of the current device's kernel launch counters
 // (FP8BS_RUNS_SLOTS 64-bit words), looked up once per device; nullptr when

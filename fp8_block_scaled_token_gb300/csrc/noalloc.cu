@@ -58,7 +58,7 @@ extern "C" fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ld
 {
     if (!x || !wq || !ws || !y || M < 1 || N < 1 || K < 1 || ldx < K)
         return FP8BS_ERR_INVALID_ARG;
-    if (flags & ~(FP8BS_FLAG_OVERLAP_PREV | FP8BS_FLAG_WEIGHTS_TILED))
+    if (flags & ~(FP8BS_FLAG_OVERLAP_PREV | FP8BS_FLAG_WEIGHTS_TILED | FP8BS_FLAG_PROLOGUE_CAST))
         return FP8BS_ERR_INVALID_ARG;
     if (M > 64 || K % 128 != 0 || N > (1 << 30) || K > (1 << 30))
         return FP8BS_ERR_UNSUPPORTED_SHAPE;

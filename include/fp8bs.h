@@ -96,6 +96,19 @@ typedef enum fp8bs_dtype {
  * read instead of 128 separate 128-byte pieces of 128 different rows. */
 #define FP8BS_FLAG_WEIGHTS_TILED 2u
 
+/* Flag for the fused entry points (fp8_blockscaled_gemm_fused, its greedy and
+ * no-allocation variants): cast the activations in the GEMM kernel's
+ * prologue, every CTA its own K blocks' token rows straight into a
+ * shared-memory cache (one kernel), wherever that cache fits (at most 16
+ * (K block, token) rows a CTA and 96 KB); elsewhere, and without the flag,
+ * the cast runs as its own kernel before the pre-quantised GEMM.  Measured on
+ * GB300, the two-kernel route is the faster one for every shape tried, 3-10 %
+ * for 1 to 16 tokens, chained with or without programmatic dependent launch:
+ * the prologue kernel holds one CTA per SM and repeats each K block's cast in
+ * every CTA that uses it.  fp8bs_fused_route reports the route for a flag
+ * set. */
+#define FP8BS_FLAG_PROLOGUE_CAST 4u
+
 /* Human-readable text of a status code (static storage, never NULL). */
 FP8BS_API const char *fp8bs_status_string(fp8bs_status status);
 
@@ -354,14 +367,16 @@ FP8BS_API fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int
                                            int *ctas, long long *units, int *split);
 
 /*
- * The route fp8_blockscaled_gemm_fused takes for this shape: *prologue = 1
- * when every CTA casts its own activation rows in the GEMM kernel's prologue
- * (one kernel), 0 when the cast runs as its own kernel into the workspace
+ * The route fp8_blockscaled_gemm_fused takes for this shape and `flags`:
+ * *prologue = 1 when every CTA casts its own activation rows in the GEMM
+ * kernel's prologue (one kernel; only with FP8BS_FLAG_PROLOGUE_CAST, where
+ * the cache fits), 0 when the cast runs as its own kernel into the workspace
  * before the pre-quantised GEMM (two kernels).  num_sms <= 0 means "the
- * current device".  The choice depends only on (M, N, K, SM count).
- * Nothing is launched.
+ * current device".  The choice depends only on (M, N, K, SM count, flags).
+ * Nothing is launched.  Flags other than the fused entry points' are
+ * rejected (FP8BS_ERR_INVALID_ARG).
  */
-FP8BS_API fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, int *prologue);
+FP8BS_API fp8bs_status fp8bs_fused_route(int M, int N, int K, int num_sms, unsigned flags, int *prologue);
 
 /*
  * The K-split schedule the GEMMs use, exposed for inspection and tests.

@@ -41,12 +41,16 @@ int main(void)
            "schedule query");
     expect(npad == 128 && tt == 4 && ctas == 152 && units == 6400 && split == 1, "schedule values at M = 512");
 
-    /* the fused entry point's route: prologue cast for the tiny workload, the
-       separate cast kernel for the square layer at 8 tokens */
+    /* the fused entry point's route: the separate cast kernel by default; with
+       the prologue-cast flag, the prologue for the tiny workload and still the
+       separate cast for the square layer at 8 tokens */
     {
         int prologue = -1;
-        expect(fp8bs_fused_route(8, 256, 512, 152, &prologue) == FP8BS_OK && prologue == 1, "tiny: prologue");
-        expect(fp8bs_fused_route(8, 5120, 5120, 152, &prologue) == FP8BS_OK && prologue == 0, "square: separate");
+        expect(fp8bs_fused_route(8, 256, 512, 152, 0, &prologue) == FP8BS_OK && prologue == 0, "tiny: separate by default");
+        expect(fp8bs_fused_route(8, 256, 512, 152, FP8BS_FLAG_PROLOGUE_CAST, &prologue) == FP8BS_OK && prologue == 1,
+               "tiny: prologue with the flag");
+        expect(fp8bs_fused_route(8, 5120, 5120, 152, FP8BS_FLAG_PROLOGUE_CAST, &prologue) == FP8BS_OK && prologue == 0,
+               "square: separate");
     }
 
     if (failures == 0)

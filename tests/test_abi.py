@@ -201,10 +201,17 @@ def test_gemm_schedule_policy(L):
 
 
 def test_fused_route_policy(L):
-    """The fused entry point casts in the GEMM prologue only when every CTA
-    has at most 16 (K block, token) rows to cast; otherwise it runs the cast
-    kernel first.  The decision is a pure function of (M, N, K, SM count)."""
-    r = lambda M, N, K, sms=152: fb.fused_route(M, N, K, sms)
+    """By default the fused entry point runs the cast kernel first; with
+    FP8BS_FLAG_PROLOGUE_CAST it casts in the GEMM prologue when every CTA has
+    at most 16 (K block, token) rows to cast.  The decision is a pure
+    function of (M, N, K, SM count, flags)."""
+    PRO = fb.FLAG_PROLOGUE_CAST
+    for M, N, K in ((8, 256, 512), (1, 5120, 5120), (2, 2048, 1024), (16, 640, 2048), (64, 5120, 5120)):
+        assert fb.fused_route(M, N, K, 152) == "separate"
+        assert fb.fused_route(M, N, K, 152, flags=fb.FLAG_OVERLAP_PREV | fb.FLAG_WEIGHTS_TILED) == "separate"
+    with pytest.raises(fb.Fp8bsError):
+        fb.fused_route(8, 256, 512, 152, flags=8)          # not a flag of the fused entry points
+    r = lambda M, N, K, sms=152: fb.fused_route(M, N, K, sms, flags=PRO)
     # the tiny workload: 8 units on 8 CTAs, one K block of 8 rows each
     assert r(8, 256, 512) == "prologue"
     # square layer: ~11 K blocks per CTA; 11 rows at M = 1, 88 at M = 8

@@ -37,7 +37,9 @@ def debug_lib_built():
 
 
 def _layer(x, wq, ws, N, work):
-    y = fb.fp8_blockscaled_gemm_fused(x, wq, ws, workspace=work, n=N)
+    # the fused entry point on its prologue-cast route where that fits (the
+    # separate cast elsewhere), and the two-kernel path
+    y = fb.fp8_blockscaled_gemm_fused(x, wq, ws, workspace=work, n=N, flags=fb.FLAG_PROLOGUE_CAST)
     xq, xs = fb.fp8_quant_act(x)
     y2 = fb.fp8_blockscaled_gemm(xq, xs, wq, ws, workspace=work, n=N)
     return y, y2

@@ -53,6 +53,17 @@ def test_fused_matches_oracle(M):
     _full_case(M, 640, 2048, 60 + M, fused=True)
 
 
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_fused_prologue_cast_matches_oracle(M):
+    """The prologue-cast route (FP8BS_FLAG_PROLOGUE_CAST) against the oracle."""
+    assert fb.fused_route(M, 640, 2048, flags=fb.FLAG_PROLOGUE_CAST) == "prologue"
+    x = synth.activations(M, 2048, seed=70 + M)
+    w = synth.weights(640, 2048, seed=71 + M)
+    ref = oracle_layer(x, w)
+    y = gpu_layer(x.cuda(), w.cuda(), fused=True, flags=fb.FLAG_PROLOGUE_CAST)
+    check_y(y, ref["y"], ref["bound"], "prologue cast M=%d" % M)
+
+
 def test_ragged_n_and_outliers():
     _full_case(8, 300, 1280, 11, w_out=0.01, x_out=0.001)
     _full_case(5, 129, 384, 12)
@@ -73,35 +84,43 @@ def test_closed_form_constant():
 
 
 def test_fused_is_bitwise_the_two_kernel_path():
-    # the first three cast in the kernel prologue (at most 16 rows per CTA),
-    # the others through the separate cast kernel
+    # by default through the separate cast kernel; with the prologue-cast flag
+    # the first three cast in the kernel prologue (at most 16 rows per CTA)
     for M, N, K, seed in ((1, 5120, 5120, 27), (2, 2048, 1024, 28), (16, 640, 2048, 29), (8, 5120, 5120, 1),
                           (33, 1000, 3072, 21), (64, 256, 512, 22), (64, 5120, 5120, 25), (16, 2048, 17408, 26)):
         x = synth.activations(M, K, seed=seed, outlier_p=0.001).cuda()
         w = synth.weights(N, K, seed=seed + 1).cuda()
         a = gpu_layer(x, w, fused=False)
         b = gpu_layer(x, w, fused=True)
+        c = gpu_layer(x, w, fused=True, flags=fb.FLAG_PROLOGUE_CAST)
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (M, N, K)
+        assert torch.equal(a.view(torch.int16), c.view(torch.int16)), (M, N, K, "prologue flag")
 
 
 def _tpad(M):
     return 16 if M <= 16 else 32 if M <= 32 else 48 if M <= 48 else 64
 
 
+@pytest.mark.parametrize("prologue", [False, True])
 @pytest.mark.parametrize("M,N,K,route", [(8, 256, 512, "prologue"), (1, 5120, 5120, "prologue"),
                                          (2, 2048, 1024, "prologue"), (16, 640, 2048, "prologue"),
                                          (8, 5120, 5120, "separate"), (33, 1000, 3072, "separate"),
                                          (64, 256, 512, "separate"), (16, 2048, 17408, "separate")])
-def test_fused_route_runs_the_intended_kernels(M, N, K, route):
+def test_fused_route_runs_the_intended_kernels(M, N, K, route, prologue):
     """Looks inside the process: the fused entry point launches exactly the
     kernels of the route its query names -- one prologue-cast GEMM, or the
-    cast kernel followed by the pre-quantised GEMM -- and nothing else."""
-    assert fb.fused_route(M, N, K) == route
+    cast kernel followed by the pre-quantised GEMM -- and nothing else.
+    `route` is the route with FP8BS_FLAG_PROLOGUE_CAST; without it the route
+    is always the separate cast."""
+    flags = fb.FLAG_PROLOGUE_CAST if prologue else 0
+    if not prologue:
+        route = "separate"
+    assert fb.fused_route(M, N, K, flags=flags) == route
     x = synth.activations(M, K, seed=M + 5).cuda()
     wq, ws = fb.fp8_quant_weight_blocks(synth.weights(N, K, seed=M + 6).cuda())
     torch.cuda.synchronize()
     with Ran() as r:
-        fb.fp8_blockscaled_gemm_fused(x, wq, ws)
+        fb.fp8_blockscaled_gemm_fused(x, wq, ws, flags=flags)
     if route == "prologue":
         assert r.launched() == {runs_gemm(MODE_FUSED, _tpad(M)): 1}
     else:

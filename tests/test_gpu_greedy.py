@@ -35,9 +35,11 @@ def check_valid_choice(token, ref, cols=None):
         assert y[m, j] + lim[m, j] >= np.max(y[m] - lim[m]), "token row %d" % m
 
 
+@pytest.mark.parametrize("prologue", [False, True])
 @pytest.mark.parametrize("M,N,K,tiled", [(8, 5120, 5120, True), (1, 2000, 1280, False), (3, 300, 512, True),
                                          (16, 4096, 1024, True), (33, 1000, 640, False), (64, 3000, 2048, True)])
-def test_greedy_matches_own_logits_and_oracle(M, N, K, tiled):
+def test_greedy_matches_own_logits_and_oracle(M, N, K, tiled, prologue):
+    flags = fb.FLAG_PROLOGUE_CAST if prologue else 0
     x_cpu = synth.activations(M, K, seed=M + 500)
     w_cpu = synth.weights(N, K, seed=M + 501, outlier_p=0.01)
     x, w = x_cpu.cuda(), w_cpu.cuda()
@@ -45,10 +47,10 @@ def test_greedy_matches_own_logits_and_oracle(M, N, K, tiled):
     y_ref = fb.fp8_blockscaled_gemm_fused(x, wq, ws, n=N)
     work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K))
     with Ran() as r:
-        token, logit, y = fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, workspace=work, n=N)
+        token, logit, y = fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, workspace=work, n=N, flags=flags)
     # the greedy instantiation of the route's GEMM is the kernel that ran
     npad = fb.gemm_schedule(M, N, K)["npad"]
-    if fb.fused_route(M, N, K) == "prologue":
+    if fb.fused_route(M, N, K, flags=flags) == "prologue":
         assert r.launched() == {runs_gemm(MODE_FUSED, npad, greedy=True): 1}
     else:
         assert r.launched() == {RUNS_QUANT_ACT: 1, runs_gemm(MODE_FP8, npad, greedy=True): 1}
@@ -57,7 +59,7 @@ def test_greedy_matches_own_logits_and_oracle(M, N, K, tiled):
     check_valid_choice(token, oracle_layer(x_cpu, w_cpu))
     # again, without storing the logits, on the same workspace (keys cleared)
     t2, l2, none = fb.fp8_blockscaled_gemm_fused_greedy(x, wq, ws, store_y=False, workspace=work,
-                                                        flags=fb.FLAG_OVERLAP_PREV, n=N)
+                                                        flags=flags | fb.FLAG_OVERLAP_PREV, n=N)
     torch.cuda.synchronize()
     assert none is None
     assert torch.equal(t2, token) and torch.equal(l2.view(torch.int32), logit.view(torch.int32))
