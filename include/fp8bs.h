@@ -202,18 +202,19 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm(const uint8_t *aq, const float *as,
 
 /*
  * The whole layer from bf16 activations: activation quantisation (as
- * fp8_quant_act) fused with the GEMM (as fp8_blockscaled_gemm).  In the GEMM
- * kernel's prologue every CTA quantises the token rows of the K blocks it
+ * fp8_quant_act) fused with the GEMM (as fp8_blockscaled_gemm).  By default
+ * the quantisation runs once as its own kernel into the workspace, followed
+ * by the pre-quantised GEMM on the same stream.  With
+ * FP8BS_FLAG_PROLOGUE_CAST, where each CTA has at most 16 (K block, token)
+ * rows to cast and its cache fits 96 KB, it runs in the GEMM kernel's
+ * prologue instead: every CTA quantises the token rows of the K blocks it
  * will use straight into a shared-memory cache in the tensor-core operand
- * layout, so the quantised activations never reach global memory.  Every CTA
- * quantises its own K blocks, so this work is replicated across the SMs; when
- * a CTA would have more than 16 (K block, token) rows to cast, or its cache
- * would exceed 96 KB, the call instead runs the quantisation once as its own
- * kernel into the workspace, followed by the pre-quantised GEMM (faster on
- * GB300 beyond that size).  Either way
+ * layout (one kernel, replicated work; slower on GB300 in every
+ * configuration measured, see the flag).  Either way
  * the result is bitwise identical to fp8_quant_act followed by
  * fp8_blockscaled_gemm.
  * x: bf16, M rows, row stride ldx elements, 16-byte aligned, ldx % 8 == 0.
+ * flags: as fp8_blockscaled_gemm, plus FP8BS_FLAG_PROLOGUE_CAST.
  * Other arguments as fp8_blockscaled_gemm.
  */
 FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused(const void *x, int ldx,
