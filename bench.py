@@ -37,6 +37,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -205,11 +206,21 @@ def gpu_query_id(dev):
     return str(dev.index if dev.index is not None else 0)
 
 
+def _code_only(text):
+    """C++ source without its comments and with whitespace runs collapsed:
+    what the compiler sees, so a comment edit does not change the hash."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash():
+    """First 16 hex digits of the sha256 of the GEMM kernel's sources, their
+    comments and whitespace removed (string literals in them hold no //)."""
     h = hashlib.sha256()
     for n in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "fp8_block_scaled_token_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fp8_block_scaled_token_gb300", "csrc", n)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

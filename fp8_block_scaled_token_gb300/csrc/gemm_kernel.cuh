@@ -18,12 +18,16 @@
 //   warp 1      MMA issuer: per 128-wide K block, four tcgen05.mma with the
 //               weights as the 128-row A operand and the tokens (padded to
 //               NPAD = 16/32/48/64/128) as the B operand, fp32 accumulator in
-//               tensor memory (4 buffers so the epilogue never stalls it).
-//   warps 2-5   promotion / epilogue: one thread per weight row reads its
-//               accumulator row (tcgen05.ld), multiplies by
+//               tensor memory (8 buffers for the 16-token tile, 4 otherwise,
+//               so the epilogue rarely stalls it).
+//   warps 2-5   promotion / epilogue (warps 2-9 from 64 tokens, two groups
+//               splitting the token columns): one thread per weight row reads
+//               its accumulator row (tcgen05.ld), multiplies by
 //               s_w[tile,kb] * s_a[m,kb] and adds into fp32 registers; at the
 //               end of a pair it stores bf16 Y, or hands its partial to the
-//               fixed-order K-split reduction.
+//               fixed-order K-split reduction (whose last contributor gathers
+//               the partials, by bulk copy into the idle ring from 32 tokens
+//               up).
 //   greedy (optional, the output layer): while storing a finished tile the
 //               epilogue warps also pick, per token, the tile's largest bf16
 //               logit (lowest column on ties); each CTA folds its tiles in
@@ -37,8 +41,8 @@
 //               weights only, and the MMA reads its B operand from the cache.
 //
 // Shared memory: [1 KB barriers and flags][ring: S stages][activation cache]
-// [activation scales][scale products]; S and the cache size are chosen per
-// launch.
+// [activation scales][per-warp scale products]; S and the cache size are
+// chosen per launch.
 //
 // Every wait is bounded; on time-out the CTA records a code in the status
 // word, drains what it has in flight, frees its tensor memory and returns.
@@ -53,9 +57,11 @@
 #include "quant_math.cuh"
 
 
-// Columns per TMEM load-and-wait in the promotion step: 64 for the 128-token
-// tile (measured: square layer M = 256 31.2 -> 29.5 us), 32 where the
-// columns allow, 16 for the 256-token tile, whose wider loads spill.
+// Columns per TMEM load-and-wait in the promotion step: 16 where the token
+// columns are split over two epilogue groups (64 tokens and up: one 64-column
+// load per unit measured slower there, 180 -> 204 ns of promotion per unit at
+// 128 tokens), 64 for a single group of 128 columns, 32 where the columns
+// allow, else 16.
 #define FP8BS_TMEM_LD_COLS(cols, groups)                                                                     \
     (((groups) != 1) ? 16 : ((cols) >= 128) ? 64 : ((cols) % 32 == 0) ? 32 : 16)
 
