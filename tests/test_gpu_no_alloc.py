@@ -8,10 +8,9 @@ Called through the C ABI and compared with the existing entry point,
 fp8_blockscaled_gemm_fused with a caller-provided workspace: both run the same
 kernels on the same schedule, so the results must be bitwise equal, on two
 calls in a row (the second call finds the scratch as the first left it); the
-result is also checked against the oracle.  The file sorts last so that, if
-it fails, a run that stops at the first failure has run every other test; it
-passes in any order, and alone in a fresh process, where its first call does
-the per-device set-up.
+result is also checked against the oracle.  Nothing here depends on test
+order: run alone in a fresh process, its first call does the per-device
+set-up of the scratch array.
 """
 import ctypes
 
