@@ -91,7 +91,7 @@ fp8bs_status ensure_smem_attr(const void *kernel, int bytes, int device, unsigne
 
 fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                           uint64_t rows, uint64_t cols, uint64_t row_stride_bytes, uint32_t box_cols,
-                          uint32_t box_rows)
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle)
 {
     std::call_once(g_encode_once, []() {
         void *fn = nullptr;
@@ -111,7 +111,7 @@ fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataTyp
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
 }

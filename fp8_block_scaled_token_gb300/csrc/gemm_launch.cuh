@@ -40,6 +40,8 @@ template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stag
         }
         ring = kSmemLimit - C::smem_bytes(0, act_chunks);
     }
+    if (C::kYStageBytes > 0 && ring > kSmemLimit - C::smem_bytes(0, 0))
+        ring = kSmemLimit - C::smem_bytes(0, 0); // room for the Y staging tile
     stages = ring / C::kStageBytes;
     if (stages > C::kMaxStages)
         stages = C::kMaxStages;
@@ -91,6 +93,19 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     }
     if (st != FP8BS_OK)
         return st;
+    // Y by TMA store (128-token tile): the tensor map needs a 16-byte aligned
+    // base and a row pitch that is a multiple of 16 bytes; otherwise the
+    // epilogue stores rows itself.
+    CUtensorMap tm_y = tm_w; // not read unless y_tma
+    int y_tma = 0;
+    if (C::kYTma && L.y != nullptr && reinterpret_cast<uintptr_t>(L.y) % 16 == 0 && L.N % 8 == 0) {
+        st = make_tmap_2d(&tm_y, L.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.M),
+                          static_cast<uint64_t>(L.N), static_cast<uint64_t>(L.N) * 2, C::kTileRows, NPAD,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != FP8BS_OK)
+            return st;
+        y_tma = 1;
+    }
 
     const WorkspaceLayout wl = workspace_layout(sh, L.M, L.K);
     uint8_t *wsb = static_cast<uint8_t *>(L.workspace);
@@ -117,6 +132,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     p.slots = reinterpret_cast<float *>(wsb + wl.slots_off);
     p.prefetch_before_wait = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
     p.w_tiled = tiled ? 1 : 0;
+    p.y_tma = y_tma;
     p.test_skip_unit = L.test_skip_unit;
     p.test_bad_unit = L.test_bad_unit;
     p.timeout_ns = L.timeout_ns;
@@ -136,7 +152,7 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (L.flags & FP8BS_FLAG_OVERLAP_PREV) ? 1 : 0;
-    return launch_status(cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_b, p));
+    return launch_status(cudaLaunchKernelEx(&cfg, kernel, tm_w, tm_b, tm_y, p));
 }
 
 // True when the fused kernel's activation cache fits for this shape.

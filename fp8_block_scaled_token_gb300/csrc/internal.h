@@ -27,10 +27,11 @@ fp8bs_status current_device(DeviceInfo *out);
 fp8bs_status ensure_smem_attr(const void *kernel, int bytes, int device, unsigned long long *done_mask);
 
 // 2-D tensor map for a row-major [rows][cols] matrix, box = box_cols x
-// box_rows elements, 128-byte swizzle, zero fill outside the matrix.
+// box_rows elements, 128-byte swizzle unless told otherwise, zero fill outside
+// the matrix on loads (stores outside it are dropped).
 fp8bs_status make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                           uint64_t rows, uint64_t cols, uint64_t row_stride_bytes, uint32_t box_cols,
-                          uint32_t box_rows);
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 fp8bs_status launch_status(cudaError_t e);
 

@@ -59,6 +59,32 @@ def test_square_layer(M):
     check_y(yv, ref["y"], ref["bound"], "square M=%d" % M)
 
 
+@pytest.mark.parametrize("M,N,K", [(512, 5120, 1024), (256, 7168, 1024), (300, 1024, 1024)])
+def test_y_tma_store_matches_row_stores(M, N, K):
+    """128-token tiles write Y through a shared-memory tile and one TMA store
+    when Y is 16-byte aligned and N a multiple of 8, else row by row.  Both
+    routes give the same bits; the TMA store writes no row past M; the result
+    matches the oracle.  Schedules: stream-K with whole and split tiles,
+    one pair per CTA, every tile split."""
+    x_cpu = synth.activations(M, K, seed=M + 740, outlier_p=0.001)
+    w_cpu = synth.weights(N, K, seed=M + 741, outlier_p=0.01)
+    wq, ws = fb.fp8_quant_weight_blocks(w_cpu.cuda())
+    xq, xs = fb.fp8_quant_act(x_cpu.cuda())
+    guard = torch.full((M + 1, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y_tma = guard[:M]                                   # 16-byte aligned: TMA store
+    flat = torch.full((M * N + 1,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y_rows = flat[1:].view(M, N)                        # 2-byte aligned only: row stores
+    assert y_tma.data_ptr() % 16 == 0 and y_rows.data_ptr() % 16 == 2
+    fb.fp8_blockscaled_gemm(xq, xs, wq, ws, y=y_tma)
+    fb.fp8_blockscaled_gemm(xq, xs, wq, ws, y=y_rows)
+    torch.cuda.synchronize()
+    assert torch.isnan(guard[M]).all(), "a row past M was written"
+    assert torch.isnan(flat[0]), "the element before Y was written"
+    assert torch.equal(y_tma.view(torch.int16), y_rows.view(torch.int16)), "TMA store and row stores differ"
+    ref = oracle_layer(x_cpu, w_cpu)
+    check_y(y_tma, ref["y"], ref["bound"], "M=%d N=%d" % (M, N))
+
+
 def test_deterministic_tiled_and_counters():
     M, N, K = 300, 1000, 2048
     x = synth.activations(M, K, seed=720, device="cuda")
