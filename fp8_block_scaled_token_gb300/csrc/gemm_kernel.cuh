@@ -210,13 +210,16 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kRegSplit = (16384 / (32 * kWarpsPerBank)) & ~7;
     static constexpr int kMaxRegs = kMinBlocks == 2 ? 160 : kRegSplit > 255 ? 255 : kRegSplit;
     static_assert(kMaxRegs <= kRegSplit || kRegSplit > 255, "the CTAs must fit in the register file");
-    // 128-token tile of the plain FP8 layer: a finished Y tile (128 weight
-    // rows x 128 tokens, bf16) is staged in shared memory as [token][row] and
-    // written by one TMA store, instead of 64 two-byte stores per thread
-    // (1.7 us per tile at 512 tokens, the promotion's time for ~10 units).
-    // The 32 KB cost the ring its sixth stage (1.5 % on its own); net, the
-    // decode pass at 128 / 256 / 512 tokens is 2.0-2.2 % faster.
-    static constexpr bool kYTma = NPAD == 128 && MODE == kModeFp8;
+    // Plain FP8 layer from 32 tokens up (not the greedy output layer): a
+    // finished Y tile (128 weight rows x NPAD tokens, bf16) is staged in
+    // shared memory as [token][row] and written by one TMA store, instead of
+    // up to 64 two-byte stores per thread (1.7 us per whole tile at 512
+    // tokens, the promotion's time for ~10 units; on the last contributor's
+    // critical path below 128 tokens).  For the 128-token tile the 32 KB cost
+    // the ring its sixth stage (1.5 % on its own).  Net, decode pass: 32 / 48
+    // / 64 tokens 1.9 / 2.4 / 1.5 % faster, 128 / 256 / 512 tokens 2.0-2.2 %;
+    // for the 16-token tile within noise, not taken.
+    static constexpr bool kYTma = NPAD >= 32 && MODE == kModeFp8;
     static constexpr int kYStageBytes = kYTma ? kTileRows * NPAD * 2 : 0;
     static constexpr int kHeader = 1024;                    // barriers and flags
     // the mbarriers, the TMEM address and two flags end below the greedy keys at 512
@@ -228,9 +231,10 @@ template <int NPAD, int MODE> struct GemmCfg {
     static_assert(kStageBytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
 
     // Dynamic shared memory of a launch (+1024 for aligning the base).
-    static constexpr int smem_bytes(int stages, int act_chunks)
+    // (ystage_bytes: kYStageBytes, or 0 for an instantiation that does not stage Y)
+    static constexpr int smem_bytes(int stages, int act_chunks, int ystage_bytes)
     {
-        return 1024 + kHeader + stages * kStageBytes + kYStageBytes + act_chunks * (kBBytes + kActScaleBytes) +
+        return 1024 + kHeader + stages * kStageBytes + ystage_bytes + act_chunks * (kBBytes + kActScaleBytes) +
                kProdBytes;
     }
 };
@@ -250,6 +254,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     // tile, the fused cast and the greedy choice serve at most 64 tokens):
     // pair index == weight tile, and no token-tile stepping is compiled in.
     constexpr bool kOneTT = NPAD == 16 || MODE == kModeFp8Fused || GREEDY;
+    constexpr bool kYStage = C::kYTma && !GREEDY; // Y through the staging tile and TMA
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -267,7 +272,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     const int S = p.stages;
     uint8_t *ring = smem + C::kHeader;
     uint16_t *ystage = reinterpret_cast<uint16_t *>(ring + S * C::kStageBytes); // [NPAD][128] bf16
-    uint8_t *act_cache = ring + S * C::kStageBytes + C::kYStageBytes;
+    uint8_t *act_cache = ring + S * C::kStageBytes + (kYStage ? C::kYStageBytes : 0);
     float *act_scale = reinterpret_cast<float *>(act_cache + p.act_chunks * C::kBBytes);
     float *prod = act_scale + p.act_chunks * NPAD; // [epilogue warp][2][kCols] s_w * s_a
 
@@ -670,7 +675,7 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
             // Every epilogue warp calls it (it holds named barriers).
             bool y_pending = false; // warp 2 lane 0: a TMA store may still read the staging tile
             auto store_y = [&](int n) {
-                if constexpr (C::kYTma && !GREEDY) {
+                if constexpr (kYStage) {
                     if (p.y_tma) {
                         if (warp == 2 && lane == 0 && y_pending)
                             bulk_wait_read_all(); // the previous tile's store is done with the buffer

@@ -24,9 +24,11 @@ constexpr int kPrologueMaxRows = 16;
 
 // Ring depth and activation-cache size of a launch; act_chunks < 0 means the
 // fused kernel's cache would not fit (the caller then quantises separately).
-template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stages, int &act_chunks)
+template <int NPAD, int MODE>
+void gemm_smem_plan(const GemmShape &sh, int &stages, int &act_chunks, bool greedy = false)
 {
     using C = GemmCfg<NPAD, MODE>;
+    const int ybytes = greedy ? 0 : C::kYStageBytes;
     act_chunks = 0;
     int ring = C::kMinBlocks == 2 ? kSharedRingBudget : kRingBudget;
     if (MODE == kModeFp8Fused) {
@@ -38,10 +40,10 @@ template <int NPAD, int MODE> void gemm_smem_plan(const GemmShape &sh, int &stag
             stages = 0;
             return;
         }
-        ring = kSmemLimit - C::smem_bytes(0, act_chunks);
+        ring = kSmemLimit - C::smem_bytes(0, act_chunks, 0);
     }
-    if (C::kYStageBytes > 0 && ring > kSmemLimit - C::smem_bytes(0, 0))
-        ring = kSmemLimit - C::smem_bytes(0, 0); // room for the Y staging tile
+    if (ybytes > 0 && ring > kSmemLimit - C::smem_bytes(0, 0, ybytes))
+        ring = kSmemLimit - C::smem_bytes(0, 0, ybytes); // room for the Y staging tile
     stages = ring / C::kStageBytes;
     if (stages > C::kMaxStages)
         stages = C::kMaxStages;
@@ -54,12 +56,12 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     static unsigned long long attr_done = 0;
     auto kernel = gemm_small_m_kernel<NPAD, MODE, GREEDY>;
     int stages = 0, act_chunks = 0;
-    gemm_smem_plan<NPAD, MODE>(sh, stages, act_chunks);
+    gemm_smem_plan<NPAD, MODE>(sh, stages, act_chunks, GREEDY);
     if (act_chunks < 0 || stages < 2)
         return FP8BS_ERR_UNSUPPORTED_SHAPE; // not reached: the fused launcher checks first
     if ((NPAD == 16 || MODE == kModeFp8Fused || GREEDY) && sh.ttiles != 1)
         return FP8BS_ERR_UNSUPPORTED_SHAPE; // not reached: these serve one token tile only
-    const int smem = C::smem_bytes(stages, act_chunks);
+    const int smem = C::smem_bytes(stages, act_chunks, GREEDY ? 0 : C::kYStageBytes);
     fp8bs_status st = ensure_smem_attr(reinterpret_cast<const void *>(kernel), kSmemLimit, dev.device, &attr_done);
     if (st != FP8BS_OK)
         return st;
@@ -93,12 +95,12 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     }
     if (st != FP8BS_OK)
         return st;
-    // Y by TMA store (128-token tile): the tensor map needs a 16-byte aligned
-    // base and a row pitch that is a multiple of 16 bytes; otherwise the
-    // epilogue stores rows itself.
+    // Y by TMA store (plain FP8 layer, 32 tokens and up): the tensor map
+    // needs a 16-byte aligned base and a row pitch that is a multiple of 16
+    // bytes; otherwise the epilogue stores rows itself.
     CUtensorMap tm_y = tm_w; // not read unless y_tma
     int y_tma = 0;
-    if (C::kYTma && L.y != nullptr && reinterpret_cast<uintptr_t>(L.y) % 16 == 0 && L.N % 8 == 0) {
+    if (C::kYTma && !GREEDY && L.y != nullptr && reinterpret_cast<uintptr_t>(L.y) % 16 == 0 && L.N % 8 == 0) {
         st = make_tmap_2d(&tm_y, L.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(L.M),
                           static_cast<uint64_t>(L.N), static_cast<uint64_t>(L.N) * 2, C::kTileRows, NPAD,
                           CU_TENSOR_MAP_SWIZZLE_NONE);

@@ -59,13 +59,15 @@ def test_square_layer(M):
     check_y(yv, ref["y"], ref["bound"], "square M=%d" % M)
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 5120, 1024), (256, 7168, 1024), (300, 1024, 1024)])
+@pytest.mark.parametrize("M,N,K", [(512, 5120, 1024), (256, 7168, 1024), (300, 1024, 1024), (33, 640, 1024),
+                                   (64, 5120, 512)])
 def test_y_tma_store_matches_row_stores(M, N, K):
-    """128-token tiles write Y through a shared-memory tile and one TMA store
-    when Y is 16-byte aligned and N a multiple of 8, else row by row.  Both
-    routes give the same bits; the TMA store writes no row past M; the result
-    matches the oracle.  Schedules: stream-K with whole and split tiles,
-    one pair per CTA, every tile split."""
+    """From 32 tokens up the plain layer writes Y through a shared-memory tile
+    and one TMA store when Y is 16-byte aligned and N a multiple of 8, else
+    row by row.  Both routes give the same bits; the TMA store writes no row
+    past M (the 48- and 64-token tiles are taller than 33 tokens); the result
+    matches the oracle.  Schedules: stream-K with whole and split tiles, one
+    pair per CTA, every tile split, K split across every SM."""
     x_cpu = synth.activations(M, K, seed=M + 740, outlier_p=0.001)
     w_cpu = synth.weights(N, K, seed=M + 741, outlier_p=0.01)
     wq, ws = fb.fp8_quant_weight_blocks(w_cpu.cuda())
