@@ -100,7 +100,7 @@ struct GemmParams {
     float *slots;            // [2 * ctas][NPAD * 128] fp32 partials
     int prefetch_before_wait;// weights may be fetched before the previous grid completes
     int w_tiled;             // weights in the tiled layout (one contiguous 16 KB run per tile)
-    int y_tma;               // 128-token tile: Y tiles leave through shared memory and a TMA store
+    int y_tma;               // Y tiles leave through shared memory and a TMA store
     int test_skip_unit;      // -1, or a unit whose stage the producer never fills
     int test_bad_unit;       // -1, or a unit the producer addresses one weight tile past the end
                              // (the FP8BS_DEBUG build's checks must catch it)
@@ -255,6 +255,13 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     // pair index == weight tile, and no token-tile stepping is compiled in.
     constexpr bool kOneTT = NPAD == 16 || MODE == kModeFp8Fused || GREEDY;
     constexpr bool kYStage = C::kYTma && !GREEDY; // Y through the staging tile and TMA
+    // Under programmatic dependent launch the next grid is released once
+    // this CTA's producer has six weight loads left to issue, not at its
+    // start: the next layer's CTAs then fetch their first ring pass while this
+    // grid finishes instead of while it streams (decode pass, M = 1 to 64:
+    // 0.2-0.9 % faster than a release at the start; a release after the last
+    // load was 4 % slower at M = 16, three loads early 0.6 % slower there).
+    constexpr int kTriggerLead = 6;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -329,9 +336,6 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (threadIdx.x == 0)
-        grid_launch_dependents();
-
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -398,7 +402,12 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
             }
             int s = pre % S;
             uint32_t ph = static_cast<uint32_t>(pre / S) & 1u;
+            bool triggered = false;
             for (int i = pre; i < nunits; ++i) {
+                if (!triggered && i >= nunits - kTriggerLead) {
+                    grid_launch_dependents();
+                    triggered = true;
+                }
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.status, kErrTimeoutProducer, p.timeout_ns))
                     break;
                 if (i != p.test_skip_unit && unit_ok(s, kb, bad(i, wt), trow)) {
@@ -424,6 +433,8 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                 }
                 step(kb, wt, trow);
             }
+            if (!triggered)
+                grid_launch_dependents(); // every weight load of this CTA is issued
             // Nothing may still be landing in shared memory when the CTA exits:
             // wait (bounded) for the last phase armed on every stage.
             for (int s = 0; s < S; ++s) {
