@@ -559,7 +559,7 @@ def sweep(weights, dev, stream, peak):
     names = {(5120, 5120): "square_decode", (34816, 5120): "mlp_up", (5120, 17408): "mlp_down",
              (7168, 5120): "attn_7168x5120"}
     for (N, K), name in names.items():
-        for M in ((1, 8, 64) if name == "square_decode" else (8,)):
+        for M in ((1, 8, 64, 128, 512) if name == "square_decode" else (8,)):
             r = PassRunner(weights, M, dev, layers=weights.of_shape(N, K))
             g = graph_of(r.run, stream)
             reps = max(1, 2000 // len(r.layers))
@@ -604,13 +604,15 @@ def sweep(weights, dev, stream, peak):
     torch.cuda.empty_cache()
     # the native block-scaled (MX) variant: activation cast + MX GEMM per
     # layer (a different numeric contract: 1x32 power-of-two scales), on 64
-    # distinct square layers and on the output layer
-    for (N, K), name, R in (((5120, 5120), "mx_square_decode", 64), (VOCAB, "mx_vocab", 2)):
+    # distinct square layers (also at 128 and 512 tokens, beside the FP8
+    # square layer's rows) and on the output layer
+    for (N, K), name, R, Ms in (((5120, 5120), "mx_square_decode", 64, (1, 8, 128, 512)),
+                                (VOCAB, "mx_vocab", 2, (1, 8))):
         mx = [fb.fp8_mx_quant_weights(synth.weights(N, K, seed=400 + i, device=dev)) for i in range(R)]
-        for M in (1, 8):
+        for M in Ms:
             x = synth.activations(M, K, seed=1, device=dev)
             xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
-            xa = torch.empty((K // 128, 512), dtype=torch.uint8, device=dev)
+            xa = torch.empty(((M + 127) // 128 * (K // 128), 512), dtype=torch.uint8, device=dev)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             work = fb.make_workspace(fb.fp8_mx_gemm_workspace_size(M, N, K), dev)
 

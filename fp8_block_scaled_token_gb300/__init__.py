@@ -383,8 +383,8 @@ def fp8_mx_quant_weights(w, wq=None, ws_atoms=None):
 
 
 def fp8_mx_quant_act(x, xq=None, xs_atoms=None, flags=0):
-    """bf16 X [M, K] (M <= 64; row stride may exceed K) -> (xq uint8 [M, K],
-    xs_atoms uint8 [K/128, 512])."""
+    """bf16 X [M, K] (M <= 512; row stride may exceed K) -> (xq uint8 [M, K],
+    xs_atoms uint8 [ceil(M/128) * K/128, 512]: atom (token tile, K block))."""
     torch = _torch()
     _need(x, torch.bfloat16, "x")
     _rows_contiguous(x, "x")
@@ -392,7 +392,7 @@ def fp8_mx_quant_act(x, xq=None, xs_atoms=None, flags=0):
     if xq is None:
         xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if xs_atoms is None:
-        xs_atoms = torch.empty((max(K // 128, 0), 512), dtype=torch.uint8, device=x.device)
+        xs_atoms = torch.empty((((M + 127) // 128) * max(K // 128, 0), 512), dtype=torch.uint8, device=x.device)
     _check("fp8_mx_quant_act", lib().fp8_mx_quant_act(_ptr(x), M, K, x.stride(0), _ptr(xq), _ptr(xs_atoms), flags,
                                                       _stream()))
     return xq, xs_atoms
@@ -415,7 +415,8 @@ def fp8_mx_gemm(aq, as_atoms, wq, ws_atoms, n, y=None, workspace=None, flags=0):
     M, K = aq.shape
     N = int(n)
     tiles = ((N + 127) // 128) * (K // 128)
-    if wq.numel() != tiles * 16384 or ws_atoms.numel() != tiles * 512 or as_atoms.numel() != (K // 128) * 512:
+    if (wq.numel() != tiles * 16384 or ws_atoms.numel() != tiles * 512 or
+            as_atoms.numel() != ((M + 127) // 128) * (K // 128) * 512):
         raise ValueError("operand shapes do not agree")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=aq.device)

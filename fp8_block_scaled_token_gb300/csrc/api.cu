@@ -170,6 +170,8 @@ GemmShape gemm_shape(int mode, int M, int N, int K, int sms)
     // a weight tile read it from L2 after the first.  (256-token tiles
     // promote 15% slower per token than 128-token ones and are not used.)
     for (int tt : {128, 64, 32}) {
+        if (mode == 3 && tt != 128)
+            break; // MX: the token scale atoms hold 128-token tiles
         const int tiles_m = (M + tt - 1) / tt;
         const long long pairs = static_cast<long long>(s.ntiles) * tiles_m;
         if (pairs <= sms && pairs * (s.kg + 16) >= static_cast<long long>(sms) * s.kg) {
@@ -599,7 +601,7 @@ fp8bs_status fp8_mx_quant_act(const void *x, int M, int K, int ldx, uint8_t *xq,
         return FP8BS_ERR_INVALID_ARG;
     if (check_flags(flags, FP8BS_FLAG_OVERLAP_PREV) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
-    if (M > 64 || K % 128 != 0 || K > (1 << 30))
+    if (M > kMaxTokens || K % 128 != 0 || K > (1 << 30))
         return FP8BS_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(xq, 16) || !aligned(xs_atoms, 16))
         return FP8BS_ERR_MISALIGNED;
@@ -619,8 +621,6 @@ fp8bs_status fp8_mx_gemm_workspace_size(int M, int N, int K, size_t *bytes)
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
-    if (M > 64)
-        return FP8BS_ERR_UNSUPPORTED_SHAPE;
     return gemm_workspace(3, M, N, K, bytes);
 }
 
@@ -633,8 +633,6 @@ fp8bs_status fp8_mx_gemm(const uint8_t *aq, const uint8_t *as_atoms, const uint8
     fp8bs_status st = check_gemm_shape(M, N, K, 128);
     if (st != FP8BS_OK)
         return st;
-    if (M > 64)
-        return FP8BS_ERR_UNSUPPORTED_SHAPE;
     if (check_flags(flags, FP8BS_FLAG_OVERLAP_PREV) != FP8BS_OK)
         return FP8BS_ERR_INVALID_ARG;
     if (!aligned(aq, 16) || !aligned(as_atoms, 16) || !aligned(wq, 16) || !aligned(ws_atoms, 16) ||

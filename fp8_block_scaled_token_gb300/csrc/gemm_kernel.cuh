@@ -152,11 +152,14 @@ template <int NPAD, int MODE> struct GemmCfg {
     // libraries alternating in one process, three boxes): eight against four
     // 1.2-1.6 % faster at M = 1 and 8; sixteen 0.3 % slower than eight; eight
     // for the 32- to 64-token tiles within +-0.7 % (not taken).
-    static constexpr int kAcc = NPAD == 16 ? 8 : NPAD == 256 ? 2 : 4;
+    // (MX at 128 tokens: two, each a whole tile segment's sum, so that they
+    // and the scale-factor columns fit the 512 columns.)
+    static constexpr int kAcc = NPAD == 16 ? 8 : (NPAD == 256 || (MODE == kModeMx && NPAD == 128)) ? 2 : 4;
     // MX: after the accumulators, 8 columns of scale factors per ring stage
     // (4 for the weight atom, 4 for the token atom).
     static constexpr int kSfCol = kAcc * NPAD;
     static constexpr int kTmemNeed = kAcc * NPAD + (kMx ? kMaxStages * 8 : 0);
+    static_assert(kTmemNeed <= 512, "tensor memory has 512 columns");
     static constexpr int kTmemCols =
         kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kQuantWarps = MODE == kModeFp8Fused ? 4 : 0;
@@ -219,7 +222,7 @@ template <int NPAD, int MODE> struct GemmCfg {
     // the ring its sixth stage (1.5 % on its own).  Net, decode pass: 32 / 48
     // / 64 tokens 1.9 / 2.4 / 1.5 % faster, 128 / 256 / 512 tokens 2.0-2.2 %;
     // for the 16-token tile within noise, not taken.
-    static constexpr bool kYTma = NPAD >= 32 && MODE == kModeFp8;
+    static constexpr bool kYTma = NPAD >= 32 && (MODE == kModeFp8 || MODE == kModeMx);
     static constexpr int kYStageBytes = kYTma ? kTileRows * NPAD * 2 : 0;
     static constexpr int kHeader = 1024;                    // barriers and flags
     // the mbarriers, the TMEM address and two flags end below the greedy keys at 512
@@ -249,7 +252,8 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
     using C = GemmCfg<NPAD, MODE>;
     static_assert(!GREEDY || NPAD <= 64, "the greedy choice keeps one key per token for at most 64 tokens");
     static_assert(MODE != kModeFp8Fused || NPAD <= 64, "the fused cast serves at most 64 tokens");
-    static_assert(MODE != kModeMx || (NPAD <= 64 && !GREEDY), "the MX layer serves at most 64 tokens");
+    static_assert(MODE != kModeMx || ((NPAD <= 64 || NPAD == 128) && !GREEDY),
+                  "the MX layer: tiles of up to 64 tokens, or 128-token tiles (whose atoms hold 128 tokens)");
     // Instantiations that only ever run one token tile (the 16-token decode
     // tile, the fused cast and the greedy choice serve at most 64 tokens):
     // pair index == weight tile, and no token-tile stepping is compiled in.
@@ -395,9 +399,10 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                         continue;
                     tma_load_2d(ring + i * C::kStageBytes + C::kWBytes, &tm_b, &full[i], kb_b * C::kChunkElems,
                                 trow_b, pol_b);
-                    if constexpr (C::kMx)
+                    if constexpr (C::kMx) // token atoms [128-token tile][K block]
                         bulk_load_1d(ring + i * C::kStageBytes + C::kWBytes + C::kBBytes + 512,
-                                     p.sfb + static_cast<long long>(kb_b) * 512, 512, &full[i], pol_b);
+                                     p.sfb + (static_cast<long long>(trow_b / 128) * kg + kb_b) * 512, 512, &full[i],
+                                     pol_b);
                 }
             }
             int s = pre % S;
@@ -424,7 +429,8 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                     if constexpr (C::kMx) {
                         uint8_t *sf = ring + s * C::kStageBytes + C::kWBytes + C::kBBytes;
                         bulk_load_1d(sf, p.sfa + (static_cast<long long>(wt) * kg + kb) * 512, 512, &full[s], pol_w);
-                        bulk_load_1d(sf + 512, p.sfb + static_cast<long long>(kb) * 512, 512, &full[s], pol_b);
+                        bulk_load_1d(sf + 512, p.sfb + (static_cast<long long>(trow / 128) * kg + kb) * 512, 512,
+                                     &full[s], pol_b);
                     }
                 }
                 if (++s == S) {

@@ -183,9 +183,9 @@ template <int MODE> bool fused_cache_fits(const GemmShape &sh)
 template <int MODE, bool GREEDY>
 fp8bs_status launch_gemm_greedy(const GemmLaunch &L, const DeviceInfo &dev, const GemmShape &sh)
 {
-    // 128-token tiles exist for the plain (non-fused, non-greedy) GEMMs only;
-    // the callers reject larger M before they get here.
-    if constexpr (MODE != kModeFp8Fused && MODE != kModeMx && !GREEDY) {
+    // 128-token tiles exist for the plain (non-fused, non-greedy) GEMMs and
+    // MX only; the callers reject larger M before they get here.
+    if constexpr (MODE != kModeFp8Fused && !GREEDY) {
         if (sh.npad == 128)
             return launch_gemm_npad<128, MODE, GREEDY>(L, dev, sh);
     }

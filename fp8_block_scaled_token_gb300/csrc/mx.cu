@@ -100,36 +100,62 @@ __global__ void __launch_bounds__(256) mx_quant_weight_kernel(const void *__rest
     }
 }
 
-// Activations: one CTA of four warps per 128-wide K group (a CTA small
-// enough to sit beside the two CTAs of the 16-token GEMM).  The CTA first
-// zeroes the group's 512-byte atom (one word per thread), then warp w casts
-// tokens w, w+4, ... < M.  Codes row-major [M][K]; the atom ends with the
-// scale bytes of tokens < M and zeros for the other rows.
+// Activations: one CTA of four warps per (128-wide K group, 128-token tile,
+// 16-row slice of the tile) (a CTA small enough to sit beside the two CTAs of
+// the 16-token GEMM).  Warp w takes rows w, w+4, ... of its slice, loads all
+// four before converting any, and writes each row's four scale bytes as the
+// one atom word they form (word 4 (r % 32) + r / 32), zero for rows >= M; the
+// last slice's CTA also zeroes the words of the rows past every slice (a tile
+// of fewer than 128 tokens has fewer slices).  Codes row-major [M][K]; atoms
+// [token tile][K group].
 constexpr int kMxCastWarps = 4;
+constexpr int kMxSliceRows = 16;                                   // rows per CTA
+constexpr int kMxRowsPerWarp = kMxSliceRows / kMxCastWarps;        // loaded together
 
-__global__ void __launch_bounds__(32 * kMxCastWarps) mx_quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
+__global__ void __maxnreg__(32) mx_quant_act_kernel(const uint16_t *__restrict__ x, int M, int K, int ldx,
                                                            uint8_t *__restrict__ xq, uint8_t *__restrict__ sf,
                                                            unsigned long long *runs)
 {
-    if (blockIdx.x == 0 && threadIdx.x == 0)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
         atomicAdd(runs + FP8BS_RUNS_MX_QUANT_ACT, 1ull);
     grid_launch_dependents();
     grid_dependency_wait();
-    const int g = blockIdx.x;
+    const int g = blockIdx.x, tt = blockIdx.y, slice = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *atom = sf + static_cast<long long>(g) * 512;
-    static_assert(32 * kMxCastWarps * 4 == 512, "one word of the atom per thread");
-    reinterpret_cast<uint32_t *>(atom)[threadIdx.x] = 0u;
-    __syncthreads(); // the zeros land before the scale bytes below
-    const int rows = M < 128 ? M : 128;
-    for (int m = warp; m < rows; m += kMxCastWarps) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(x + static_cast<long long>(m) * ldx + g * 128 + lane * 4);
-        uint32_t byte;
-        const uint32_t codes = mx_quant_row128(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y), &byte);
-        *reinterpret_cast<uint32_t *>(xq + static_cast<long long>(m) * K + g * 128 + lane * 4) = codes;
-        if ((lane & 7) == 0)
-            atom[sf_atom_offset(m, lane >> 3)] = static_cast<uint8_t>(byte);
+    uint8_t *atom = sf + (static_cast<long long>(tt) * (K / 128) + g) * 512;
+    uint32_t *const words = reinterpret_cast<uint32_t *>(atom);
+    const int r0 = slice * kMxSliceRows + warp; // this warp's rows r0, r0 + 4, ... of the tile
+    uint2 raw[kMxRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kMxRowsPerWarp; ++i) {
+        const int m = tt * 128 + r0 + kMxCastWarps * i;
+        raw[i] = make_uint2(0u, 0u);
+        if (m < M) // whole warp
+            raw[i] = *reinterpret_cast<const uint2 *>(x + static_cast<long long>(m) * ldx + g * 128 + lane * 4);
     }
+#pragma unroll
+    for (int i = 0; i < kMxRowsPerWarp; ++i) {
+        const int r = r0 + kMxCastWarps * i;
+        const int m = tt * 128 + r;
+        uint32_t word = 0u;
+        if (m < M) { // whole warp
+            uint32_t byte;
+            const uint32_t codes =
+                mx_quant_row128(bf16_lo(raw[i].x), bf16_hi(raw[i].x), bf16_lo(raw[i].y), bf16_hi(raw[i].y), &byte);
+            *reinterpret_cast<uint32_t *>(xq + static_cast<long long>(m) * K + g * 128 + lane * 4) = codes;
+            // the bytes of K blocks 0-3 sit in lanes 0, 8, 16, 24
+            word = byte | (__shfl_sync(0xffffffffu, byte, 8) << 8) | (__shfl_sync(0xffffffffu, byte, 16) << 16) |
+                   (__shfl_sync(0xffffffffu, byte, 24) << 24);
+        }
+        if (lane == 0)
+            words[sf_atom_offset(r, 0) >> 2] = word;
+    }
+    // words of the rows no slice covers (a tile of fewer than 128 tokens):
+    // word w holds row 32 (w % 4) + w / 4
+    static_assert(32 * kMxCastWarps == 128, "one atom word per thread");
+    const int wrow = 32 * static_cast<int>(threadIdx.x & 3) + static_cast<int>(threadIdx.x >> 2);
+    if (slice == static_cast<int>(gridDim.z) - 1 && wrow >= (slice + 1) * kMxSliceRows)
+        words[threadIdx.x] = 0u;
 }
 
 fp8bs_status launch_mx_quant_weights(const void *w, int wtype, int N, int K, uint8_t *wq, uint8_t *sf,
@@ -149,7 +175,9 @@ fp8bs_status launch_mx_quant_act(const void *x, int M, int K, int ldx, uint8_t *
                                  cudaStream_t stream, const DeviceInfo &dev)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(K / 128), 1, 1);
+    const int tile_rows = M < 128 ? M : 128;
+    cfg.gridDim = dim3(static_cast<unsigned>(K / 128), static_cast<unsigned>((M + 127) / 128),
+                       static_cast<unsigned>((tile_rows + kMxSliceRows - 1) / kMxSliceRows));
     cfg.blockDim = dim3(32 * kMxCastWarps, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -301,12 +301,13 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_fused_noalloc(const void *x, int ldx
  *       ceil(N/128) * 128 * K bytes, rows past N zero;
  *   ws_atoms: ceil(N/128) * (K/128) atoms, atom (nb, kb) at
  *       (nb * (K/128) + kb) * 512, rows past N zero.  Both 16-byte aligned.
- * fp8_mx_quant_act: x bf16, M rows (1..64), row stride ldx (>= K, % 8 == 0),
- *   16-byte aligned -> xq u8 [M][K] (16-byte aligned), xs_atoms: K/128
- *   atoms, atom kb at kb * 512, token rows M..127 written as zero.  flags: 0
+ * fp8_mx_quant_act: x bf16, M rows (1..512), row stride ldx (>= K, % 8 == 0),
+ *   16-byte aligned -> xq u8 [M][K] (16-byte aligned), xs_atoms:
+ *   ceil(M/128) * (K/128) atoms, atom (tt, kb) of tokens tt*128.. at
+ *   (tt * (K/128) + kb) * 512, token rows past M written as zero.  flags: 0
  *   or FP8BS_FLAG_OVERLAP_PREV (programmatic dependent launch; x is read
  *   after the previous kernel completes).
- * fp8_mx_gemm: y bf16 [M][N] from those operands, 1 <= M <= 64, K % 128 == 0;
+ * fp8_mx_gemm: y bf16 [M][N] from those operands, 1 <= M <= 512, K % 128 == 0;
  *   same swap-AB / TMA / split-K pipeline and the same workspace contract as
  *   fp8_blockscaled_gemm (size from fp8_mx_gemm_workspace_size).  flags: 0
  *   or FP8BS_FLAG_OVERLAP_PREV (the weights and their atoms may be streamed

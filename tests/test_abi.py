@@ -113,18 +113,18 @@ def test_mx_validation(L):
     assert q(A16, 0, 256, 160, A16, A16, S) == SHAPE                      # K % 128
     assert q(A16, 0, 256, 512, A16, P(0x10008), S) == MISALIGNED          # atoms 16-byte aligned
     a = L.fp8_mx_quant_act
-    assert a(A16, 65, 512, 512, A16, A16, 0, S) == SHAPE                  # at most 64 tokens
+    assert a(A16, 513, 512, 512, A16, A16, 0, S) == SHAPE                 # at most 512 tokens
     assert a(A16, 8, 512, 256, A16, A16, 0, S) == INVALID                 # ldx < K
     assert a(A16, 8, 512, 512, A16, A16, 2, S) == INVALID                 # unknown flag
     assert a(A16, 8, 512, 512, A1, A16, 0, S) == MISALIGNED
     g = L.fp8_mx_gemm
-    assert g(A16, A16, A16, A16, A16, 65, 256, 512, A16, 1 << 20, 0, S) == SHAPE
+    assert g(A16, A16, A16, A16, A16, 513, 256, 512, A16, 1 << 20, 0, S) == SHAPE
     assert g(A16, A16, A16, A16, A16, 8, 256, 384 + 64, A16, 1 << 20, 0, S) == SHAPE
     assert g(A16, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 2, S) == INVALID  # tiled is implied
     assert g(A16, P(0x10004), A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == MISALIGNED
     assert g(NUL, A16, A16, A16, A16, 8, 256, 512, A16, 1 << 20, 0, S) == INVALID
     sz = ctypes.c_size_t(3)
-    assert L.fp8_mx_gemm_workspace_size(65, 256, 512, ctypes.byref(sz)) == SHAPE and sz.value == 0
+    assert L.fp8_mx_gemm_workspace_size(513, 256, 512, ctypes.byref(sz)) == SHAPE and sz.value == 0
 
 
 def test_split_plan_partitions_units(L):

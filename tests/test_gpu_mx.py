@@ -108,7 +108,7 @@ def test_mx_quant_edge_values():
     assert np.array_equal(atoms_to_bytes(xa, N, K), s2)
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (8, 5120), (13, 1280), (64, 2048)])
+@pytest.mark.parametrize("M,K", [(1, 128), (8, 5120), (13, 1280), (64, 2048), (129, 256), (300, 1024), (512, 512)])
 def test_mx_quant_act_bit_exact(M, K):
     x = synth.activations(M, K, seed=M + 21, outlier_p=0.001)
     with Ran() as r:
@@ -117,7 +117,9 @@ def test_mx_quant_act_bit_exact(M, K):
     codes, sb = _oracle_quant(x)
     assert np.array_equal(xq.cpu().numpy(), codes)
     assert np.array_equal(atoms_to_bytes(xa, M, K), sb)
-    assert not atoms_to_bytes(xa, 128, K)[M:].any(), "token rows past M must be zero"
+    padded = (M + 127) // 128 * 128                       # one atom per 128-token tile and K block
+    assert xa.shape[0] == padded // 128 * (K // 128)
+    assert not atoms_to_bytes(xa, padded, K)[M:].any(), "token rows past M must be zero"
 
 
 def _mx_layer(M, N, K, seed, x_out=0.0, w_out=0.0):
@@ -145,11 +147,15 @@ def test_mx_gemm_smallest():
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 256, 512), (1, 640, 1024), (13, 300, 1280), (33, 1000, 2048),
-                                   (64, 384, 1024), (8, 5120, 5120), (1, 5120, 5120), (8, 512, 17408)])
+                                   (64, 384, 1024), (8, 5120, 5120), (1, 5120, 5120), (8, 512, 17408),
+                                   (65, 640, 1024), (128, 1000, 2048), (300, 5120, 1024), (512, 640, 512),
+                                   (256, 7168, 1024)])
 def test_mx_gemm_matches_oracle(M, N, K):
+    """Above 64 tokens the 128-token tile (stream-K over token-tile pairs, or
+    one pair per CTA), its token scale atoms one per 128-token tile."""
     xq, xa, wq, wa, y_ref, bound = _mx_layer(M, N, K, seed=M + N, x_out=0.001, w_out=0.01)
     work = fb.make_workspace(fb.fp8_mx_gemm_workspace_size(M, N, K))
-    npad = 16 if M <= 16 else 32 if M <= 32 else 48 if M <= 48 else 64
+    npad = 16 if M <= 16 else 32 if M <= 32 else 48 if M <= 48 else 64 if M <= 64 else 128
     with Ran() as r:
         y = fb.fp8_mx_gemm(xq, xa, wq, wa, N, workspace=work)
     assert r.launched() == {runs_gemm(MODE_MX, npad): 1}
@@ -171,10 +177,22 @@ def test_mx_gemm_deterministic_and_overlap_flag():
 
 
 def test_mx_host_errors():
-    x = synth.activations(65, 256, seed=1).cuda()
+    x = synth.activations(513, 256, seed=1).cuda()
     with pytest.raises(fb.Fp8bsError) as e:
         fb.fp8_mx_quant_act(x)
     assert e.value.code == 2
     with pytest.raises(fb.Fp8bsError) as e:
-        fb.fp8_mx_gemm_workspace_size(65, 256, 256)
+        fb.fp8_mx_gemm_workspace_size(513, 256, 256)
     assert e.value.code == 2
+
+
+def test_mx_large_m_reruns_bitwise():
+    """128-token tiles with K split across CTAs: ten reruns give the same bits."""
+    M, N, K = 300, 1024, 4096
+    xq, xa, wq, wa, _, _ = _mx_layer(M, N, K, seed=11)
+    work = fb.make_workspace(fb.fp8_mx_gemm_workspace_size(M, N, K))
+    outs = [fb.fp8_mx_gemm(xq, xa, wq, wa, N, workspace=work) for _ in range(10)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert fb.workspace_status(work) == 0
