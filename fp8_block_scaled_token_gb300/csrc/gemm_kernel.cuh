@@ -213,16 +213,17 @@ template <int NPAD, int MODE> struct GemmCfg {
     static constexpr int kRegSplit = (16384 / (32 * kWarpsPerBank)) & ~7;
     static constexpr int kMaxRegs = kMinBlocks == 2 ? 160 : kRegSplit > 255 ? 255 : kRegSplit;
     static_assert(kMaxRegs <= kRegSplit || kRegSplit > 255, "the CTAs must fit in the register file");
-    // Plain FP8 layer from 32 tokens up (not the greedy output layer): a
-    // finished Y tile (128 weight rows x NPAD tokens, bf16) is staged in
-    // shared memory as [token][row] and written by one TMA store, instead of
-    // up to 64 two-byte stores per thread (1.7 us per whole tile at 512
-    // tokens, the promotion's time for ~10 units; on the last contributor's
-    // critical path below 128 tokens).  For the 128-token tile the 32 KB cost
-    // the ring its sixth stage (1.5 % on its own).  Net, decode pass: 32 / 48
-    // / 64 tokens 1.9 / 2.4 / 1.5 % faster, 128 / 256 / 512 tokens 2.0-2.2 %;
-    // for the 16-token tile within noise, not taken.
-    static constexpr bool kYTma = NPAD >= 32 && (MODE == kModeFp8 || MODE == kModeMx);
+    // Plain FP8 and MX layers (not the greedy output layer): a finished Y
+    // tile (128 weight rows x NPAD tokens, bf16) is staged in shared memory as
+    // [token][row] and written by one TMA store, instead of up to 64
+    // two-byte stores per thread (1.7 us per whole tile at 512 tokens, the
+    // promotion's time for ~10 units; on the last contributor's critical path
+    // below 128 tokens).  For the 128-token tile the 32 KB cost the ring its
+    // sixth stage (1.5 % on its own); the 16-token tile's 4 KB fit beside
+    // its two CTAs' rings.  Net, decode pass: 1 / 4 / 8 / 16 tokens 0.4 /
+    // 0.4 / 0.9 / 1.5 % faster, 32 / 48 / 64 tokens 1.9 / 2.4 / 1.5 %, 128 /
+    // 256 / 512 tokens 2.0-2.2 %.
+    static constexpr bool kYTma = MODE == kModeFp8 || MODE == kModeMx;
     static constexpr int kYStageBytes = kYTma ? kTileRows * NPAD * 2 : 0;
     static constexpr int kHeader = 1024;                    // barriers and flags
     // the mbarriers, the TMEM address and two flags end below the greedy keys at 512

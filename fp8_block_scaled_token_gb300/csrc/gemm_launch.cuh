@@ -95,9 +95,9 @@ fp8bs_status launch_gemm_npad(const GemmLaunch &L, const DeviceInfo &dev, const 
     }
     if (st != FP8BS_OK)
         return st;
-    // Y by TMA store (plain FP8 layer, 32 tokens and up): the tensor map
-    // needs a 16-byte aligned base and a row pitch that is a multiple of 16
-    // bytes; otherwise the epilogue stores rows itself.
+    // Y by TMA store (plain FP8 and MX layers): the tensor map needs a
+    // 16-byte aligned base and a row pitch that is a multiple of 16 bytes;
+    // otherwise the epilogue stores rows itself.
     CUtensorMap tm_y = tm_w; // not read unless y_tma
     int y_tma = 0;
     if (C::kYTma && !GREEDY && L.y != nullptr && reinterpret_cast<uintptr_t>(L.y) % 16 == 0 && L.N % 8 == 0) {
