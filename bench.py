@@ -86,6 +86,14 @@ def mx_bytes(M, N, K):
     return N * K + N * K // 32 + 2 * M * K + 2 * M * N
 
 
+def pass_workload(M):
+    """The decode-pass workload of the JSON line's config (both arms)."""
+    return {"workload": "decode_pass M=%d: 256 GEMMs cycling %s (N x K, 64 distinct weights each) "
+                        "+ the 248320x5120 output layer" % (M, ", ".join("%dx%d" % s for s in PASS_SHAPES)),
+            "M": M, "gemms_per_step": len(pass_layers_shapes()),
+            "weight_bytes": sum(N * K for N, K in pass_layers_shapes())}
+
+
 def pass_layers_shapes():
     """(N, K) of the 257 GEMMs of one decode pass, in order."""
     return [PASS_SHAPES[i % 4] for i in range(4 * PASS_REPEAT)] + [VOCAB]
@@ -507,9 +515,7 @@ def run_pass(args, world, rank, dev):
             "us_per_gemm": round(t_max / steps / n_gemm * 1e6, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3xe4m3->f32",
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
-            "config": {"workload": "decode_pass M=%d: 256 GEMMs cycling %s (N x K, 64 distinct weights each) "
-                                   "+ the 248320x5120 output layer" % (M, ", ".join("%dx%d" % s for s in PASS_SHAPES)),
-                       "M": M, "gemms_per_step": n_gemm, "weight_bytes": sum(N * K for N, K in pass_layers_shapes()),
+            "config": {**pass_workload(M),
                        "kernel": "fp8_blockscaled_gemm_fused (activation cast + swap-AB tcgen05 split-K GEMM)",
                        "weights": "E4M3 tiled layout (one contiguous 16 KB run per 128x128 tile)",
                        "l2": "inputs larger than L2: 22.4 GB of distinct weights per step",
@@ -739,11 +745,12 @@ def run_reference(args, world, rank):
     if args.workload == "decode_pass":
         M = args.m or 8
         shapes = list(PASS_SHAPES) + [VOCAB]
-        wl = "decode_pass M=%d" % M
+        config = pass_workload(M)
     else:
         cfg = workload(args.workload, args.m)
         M, shapes = cfg["M"], [(cfg["N"], cfg["K"])]
-        wl = "%s M=%d N=%d K=%d" % (args.workload, M, cfg["N"], cfg["K"])
+        config = {"workload": "%s M=%d N=%d K=%d" % (args.workload, M, cfg["N"], cfg["K"]), "M": M, "N": cfg["N"],
+                  "K": cfg["K"]}
     # size each step so that the warm-up and timed steps together stay
     # within about two minutes
     budget = 120.0 / max(1, args.steps + args.warmup)
@@ -759,7 +766,7 @@ def run_reference(args, world, rank):
             "warmup": args.warmup, "ms_per_step": round(el / max(1, args.steps) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,0.02) weights, N(0,1) bf16 activations)",
-            "config": {"workload": wl, "M": M},
+            "config": config,
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": mix.threads,
                              "sample": "each step: " + mix.describe()},
