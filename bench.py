@@ -21,8 +21,12 @@ shape alone (64 distinct weights cycled), the output layer at M = 1 and 8
 the pass at M = 1 ... 512.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode_pass|square_decode|mlp_up|mlp_down|vocab|tiny]
+                  [--workload decode_pass|square_decode|mlp_up|mlp_down|vocab|tiny
+                              |mx_<layer>]
                   [--m M] [--no-sweep] [--out-dir DIR]
+
+``--workload mx_<layer>`` (mx_square_decode, ...) times the same layer in the
+MX variant (its activation cast + MX GEMM per layer; our arm only).
 
 Multi-GPU (torchrun): each rank runs its own replica on its own GPU (the
 layer needs no exchange between GPUs); the barrier + max-over-ranks timing
@@ -61,8 +65,9 @@ VOCAB = (248320, 5120)
 
 # ---------------------------------------------------------------- workloads
 def workload(name, m_override=None):
+    """A layer workload; ``mx_<name>`` is the same layer in the MX variant."""
     from fp8_block_scaled_token_gb300 import synth
-    cfg = dict(synth.WORKLOADS[name])
+    cfg = dict(synth.WORKLOADS[name[3:] if name.startswith("mx_") else name])
     if m_override:
         cfg["M"] = m_override
     return cfg
@@ -656,22 +661,33 @@ def run_layer(args, world, rank, dev):
     from fp8_block_scaled_token_gb300 import synth
     cfg = workload(args.workload, args.m)
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    mx = args.workload.startswith("mx_")  # the MX variant: its cast + MX GEMM per layer
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 1024 * 1024
     R = max(2, min(64, math.ceil(4 * l2 / (N * K))))
     layers = []
     for i in range(R):
         w = synth.weights(N, K, seed=100 + i, outlier_p=cfg.get("w_outlier_p", 0.0), device=dev)
-        layers.append((N, K) + fb.fp8_quant_weight_blocks(w, tiled=True))
+        layers.append((N, K) + (fb.fp8_mx_quant_weights(w) if mx else fb.fp8_quant_weight_blocks(w, tiled=True)))
         del w
     x = synth.activations(M, K, seed=cfg["seed"], outlier_p=cfg.get("x_outlier_p", 0.0), device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    work = fb.make_workspace(fb.fp8_blockscaled_gemm_workspace_size(M, N, K), dev)
+    work = fb.make_workspace((fb.fp8_mx_gemm_workspace_size if mx else fb.fp8_blockscaled_gemm_workspace_size)(M, N, K),
+                             dev)
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    xa = torch.empty(((M + 127) // 128 * (K // 128), 512), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
+
+    def layer(xin, wq, ws, flags):
+        if mx:
+            fb.fp8_mx_quant_act(xin, xq=xq, xs_atoms=xa, flags=flags)
+            fb.fp8_mx_gemm(xq, xa, wq, ws, N, y=y, workspace=work, flags=flags)
+        else:
+            fb.fp8_blockscaled_gemm_fused(xin, wq, ws, y=y, workspace=work, flags=flags, n=N)
 
     def ring():
         for _, _, wq, ws in layers:
-            fb.fp8_blockscaled_gemm_fused(x, wq, ws, y=y, workspace=work, flags=fb.FLAG_OVERLAP_PREV, n=N)
+            layer(x, wq, ws, fb.FLAG_OVERLAP_PREV)
 
     for _ in range(max(1, args.warmup // R + 1)):
         ring()
@@ -689,7 +705,7 @@ def run_layer(args, world, rank, dev):
     t_max = max_over_ranks(elapsed, world)
     if fb.workspace_status(work) != 0:
         raise RuntimeError("device-side timeout in the timed region")
-    nbytes = algorithmic_bytes(M, N, K)
+    nbytes = mx_bytes(M, N, K) if mx else algorithmic_bytes(M, N, K)
     peak, peak_kind = measured_peaks()
     achieved = nbytes / (elapsed / steps) / 1e9
 
@@ -703,7 +719,7 @@ def run_layer(args, world, rank, dev):
     for i in range(e2e_steps):
         x_dev.copy_(x_host, non_blocking=True)
         _, _, wq, ws = layers[i % R]
-        fb.fp8_blockscaled_gemm_fused(x_dev, wq, ws, y=y, workspace=work, n=N)
+        layer(x_dev, wq, ws, 0)
         y_host.copy_(y, non_blocking=True)
     e.record()
     torch.cuda.synchronize()
@@ -711,7 +727,7 @@ def run_layer(args, world, rank, dev):
     e2e_s = max_over_ranks(s.elapsed_time(e) / 1e3, world)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not mx:
         gbs, threads, sample = oracle_rate(M, [(N, K)], seconds=args.cpu_seconds, seed=cfg["seed"])
         cpu = {"value": round(gbs, 6), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
     if rank == 0:
@@ -726,7 +742,8 @@ def run_layer(args, world, rank, dev):
                        "timing": "CUDA graph of %d launches replayed; PDL between launches; CUDA events" % R,
                        "parallelism": "replica per GPU" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": profiled_traffic("M%d_N%d_K%d" % (M, N, K)),
+                         "frac": round(achieved / peak, 4),
+                         "traffic": None if mx else profiled_traffic("M%d_N%d_K%d" % (M, N, K)),
                          "peak_kind": peak_kind, "bytes_per_launch": nbytes,
                          "launch_us": round(elapsed / steps * 1e6, 4)},
             "cpu_baseline": cpu,
@@ -742,6 +759,9 @@ def run_layer(args, world, rank, dev):
 def run_reference(args, world, rank):
     if rank != 0:
         return
+    if args.workload.startswith("mx_"):
+        raise SystemExit("bench.py: the reference arm times the oracle of the FP8 block-scaled layer; "
+                         "the MX variant is a different numeric contract")
     if args.workload == "decode_pass":
         M = args.m or 8
         shapes = list(PASS_SHAPES) + [VOCAB]
