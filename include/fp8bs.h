@@ -181,15 +181,19 @@ FP8BS_API fp8bs_status fp8_blockscaled_gemm_workspace_size(int M, int N, int K, 
  * aq: u8 [M][K], 16-byte aligned.   as: fp32, laid out as fp8_quant_act writes
  * it for this M ([M][K/128] up to 16 tokens, [K/128][M] above).
  * wq: u8 [N][K], 16-byte aligned.   ws: fp32 [ceil(N/128)][K/128].
- * y : bf16 [M][N], 2-byte aligned.
+ * y : bf16 [M][N], 2-byte aligned.  With y 16-byte aligned and N % 8 == 0
+ *     finished Y tiles leave through shared memory and one TMA store each
+ *     (faster); otherwise the kernel stores them row by row.  Same bits.
  * 1 <= M <= 512, N >= 1, K >= 128, K % 128 == 0.  Up to 64 tokens the
  * token tile is 16, 32, 48 or 64 wide and K is split across every SM; above
  * 64 tokens (the larger-M, chunked-prefill regime, where the pages note that
  * the work turns from memory- to compute-bound: "Kernel-Level Optimisations
- * for LLM Inference and Training", "Start with the bound") the tokens are
- * cut into tiles of up to 128 and each CTA computes one 128-row weight tile
- * for one token tile over the whole K, splitting K only when N is too small
- * to occupy half of the SMs that way.
+ * for LLM Inference and Training", "Start with the bound") the work is cut
+ * into (token tile, 128-row weight tile) pairs: with at least as many
+ * 128-token pairs as SMs, or with too few pairs to keep the SMs busy, K is
+ * split over all the pairs' units (stream-K); otherwise each CTA computes
+ * one pair over the whole K, with the widest token tile (128, 64 or 32)
+ * whose pairs fit on the SMs (fp8bs_gemm_schedule reports the choice).
  * workspace: device, 256-byte aligned, >= fp8_blockscaled_gemm_workspace_size.
  * flags: any of FP8BS_FLAG_OVERLAP_PREV, FP8BS_FLAG_WEIGHTS_TILED (then wq is
  * in the tiled layout of fp8_quant_weight_blocks_tiled).
