@@ -367,7 +367,9 @@ FP8BS_API fp8bs_status fp8bs_workspace_status(void *workspace, int clear, int *c
  * then the 128-row weight tile) and whether K is split across CTAs
  * (*split = 1: the fixed-order exchange runs; 0: every CTA owns whole
  * (token tile, weight tile) pairs).  num_sms <= 0 means "the current
- * device".  Nothing is launched.
+ * device".  Nothing is launched.  (fp8_mx_gemm follows the same rules
+ * except that above 64 tokens its token tile is always 128 wide: a token
+ * scale atom covers 128 tokens.)
  */
 FP8BS_API fp8bs_status fp8bs_gemm_schedule(int M, int N, int K, int num_sms, int *npad, int *token_tiles,
                                            int *ctas, long long *units, int *split);
