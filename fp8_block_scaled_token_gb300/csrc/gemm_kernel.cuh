@@ -841,14 +841,16 @@ __global__ void __maxnreg__((GemmCfg<NPAD, MODE>::kMaxRegs))
                                 sc[j] = sw * (MODE == kModeFp8Fused ? sa_c[c * kLd + j]
                                                                     : __shfl_sync(0xffffffffu, sa_l, (c * kLd + j) & 31));
                         }
+                        if constexpr (C::kTileAcc) {
 #pragma unroll
-                        for (int j = 0; j < kLd; ++j) {
-                            const int m = c * kLd + j;
-                            const float d = __uint_as_float(r[j]);
-                            if (C::kTileAcc)
-                                acc[m] = d;
-                            else
-                                acc[m] = fmaf(sc[j], d, acc[m]);
+                            for (int j = 0; j < kLd; ++j)
+                                acc[c * kLd + j] = __uint_as_float(r[j]);
+                        } else {
+                            // two columns per packed multiply-add
+#pragma unroll
+                            for (int j = 0; j < kLd; j += 2)
+                                fma2(acc[c * kLd + j], acc[c * kLd + j + 1], sc[j], sc[j + 1], __uint_as_float(r[j]),
+                                     __uint_as_float(r[j + 1]));
                         }
                     };
                     if constexpr (kLd < 64 && kNLd > 1) {

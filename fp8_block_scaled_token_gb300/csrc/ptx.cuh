@@ -69,6 +69,21 @@ __device__ __forceinline__ void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// d0 = fma(a0, b0, d0), d1 = fma(a1, b1, d1) as one packed instruction
+// (fma.rn.f32x2: each lane one fp32 fused multiply-add, round to nearest,
+// the same result as two fmaf).
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Orders this thread's view of global memory (generic proxy) before its later
 // bulk copies from global memory (async proxy).
 __device__ __forceinline__ void fence_proxy_async_global()
