@@ -84,6 +84,19 @@ __device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, f
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// d0 += a0, d1 += a1 as one packed instruction (add.rn.f32x2, the same
+// result as two fp32 additions).
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1)
+{
+    asm("{\n\t.reg .b64 ra, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "add.rn.f32x2 rc, rc, ra;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
 // Orders this thread's view of global memory (generic proxy) before its later
 // bulk copies from global memory (async proxy).
 __device__ __forceinline__ void fence_proxy_async_global()
