@@ -63,3 +63,17 @@ def test_decode_pass_accounting():
     assert weights == 64 * (5120 * 5120 + 34816 * 5120 + 5120 * 17408 + 7168 * 5120) + 248320 * 5120
     assert abs(weights / 1e9 - 22.41) < 0.01
     assert bench.pass_bytes(8) == sum(bench.algorithmic_bytes(8, N, K) for N, K in shapes)
+
+
+def test_workload_configs():
+    """Both arms of the JSON line name the decode pass with the same config
+    (one helper builds it); ``mx_<layer>`` is the same layer in the MX variant,
+    whose bytes count one scale byte per 32 K per weight row instead of the
+    fp32 block scales and activation scales."""
+    c = bench.pass_workload(8)
+    assert c["M"] == 8 and c["gemms_per_step"] == 257
+    assert c["weight_bytes"] == sum(N * K for N, K in bench.pass_layers_shapes())
+    assert c["workload"].startswith("decode_pass M=8: 256 GEMMs cycling 5120x5120, 34816x5120")
+    assert bench.workload("mx_square_decode", 512) == dict(bench.workload("square_decode"), M=512)
+    assert bench.workload("mx_mlp_up") == bench.workload("mlp_up")
+    assert bench.mx_bytes(8, 5120, 5120) == 26214400 + 26214400 // 32 + 81920 + 81920
