@@ -19,7 +19,8 @@
 //               weights as the 128-row A operand and the tokens (padded to
 //               NPAD = 16/32/48/64/128) as the B operand, fp32 accumulator in
 //               tensor memory (8 buffers for the 16-token tile, 4 otherwise,
-//               so the epilogue rarely stalls it).
+//               so the epilogue rarely stalls it; 2 whole-segment sums for
+//               the MX 128-token tile).
 //   warps 2-5   promotion / epilogue (warps 2-9 from 64 tokens, two groups
 //               splitting the token columns): one thread per weight row reads
 //               its accumulator row (tcgen05.ld), multiplies by
